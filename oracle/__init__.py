@@ -1,0 +1,10 @@
+"""CPU fp64 oracle (test infrastructure only; see ``kd_oracle``)."""
+from .kd_oracle import (  # noqa: F401
+    dense_teacher_grid,
+    kd_backward,
+    kd_forward,
+    logsumexp_rows,
+    mean_loss,
+    student_logits,
+    teacher_log_probs,
+)

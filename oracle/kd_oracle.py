@@ -1,0 +1,164 @@
+"""CPU fp64 oracle for the top-K KL distillation loss on a student output head.
+
+TEST INFRASTRUCTURE ONLY. This module is imported by ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``. The
+product (the CUDA library and its Python binding) never imports or calls it,
+and it shares no code with that path: it is a plain, slow, obviously correct
+restatement of what the method computes, written with numpy in float64.
+
+What it restates (source: "Efficient Knowledge Distillation for LLMs: Offline
+Top-K Logits and a Fused Chunked KL Loss" and the blog post "Making Knowledge
+Distillation Cheap Enough to Run at Scale"):
+
+* The teacher is known only through its cached top-K (token id, logit) pairs
+  per position (blog, "Two systems changes", offline distillation paragraph).
+  Its distribution is the softmax of those K logits; every other token has
+  probability zero. This is the teacher grid the dense-KL bullet rebuilds
+  "from the cached top-100 logits".
+* The student distribution is the softmax of the full-vocabulary logits
+  Z = H W^T that the output projection produces (blog, fused chunked KL
+  bullet: the projection from hidden states to logits is part of the loss).
+* The loss per position is KL(teacher || student); the three variants in the
+  blog (dense, forward-chunked, fused chunked) are stated to be mathematically
+  equivalent, so the plain dense definition is the oracle for all of them.
+* The reported loss is the mean over counted (unmasked) positions.
+
+Readings where the pages are silent (each is listed with its reason in the
+design notes): both distributions use the same temperature T (student
+softmax(Z/T), teacher softmax(t/T)); there is no T^2 factor; ``lse`` is the
+natural-log logsumexp of Z/T; a duplicated teacher id is one grid entry
+whose probability is the sum of its cached entries (as in the dense teacher
+grid); masked rows give zero loss and zero gradient and their teacher entries
+are never read; with no counted rows the mean is 0.
+
+Row blocks (``row_chunk``) exist only to bound memory: every row is computed
+independently and the same way whatever the block size.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "teacher_log_probs",
+    "student_logits",
+    "logsumexp_rows",
+    "kd_forward",
+    "kd_backward",
+    "mean_loss",
+    "dense_teacher_grid",
+]
+
+
+def logsumexp_rows(a: np.ndarray) -> np.ndarray:
+    """Natural-log logsumexp along the last axis, max-shifted (fp64)."""
+    m = np.max(a, axis=-1, keepdims=True)
+    return (m + np.log(np.sum(np.exp(a - m), axis=-1, keepdims=True)))[..., 0]
+
+
+def teacher_log_probs(t_rows: np.ndarray, T: float) -> np.ndarray:
+    """log p_k = t_k/T - logsumexp_k(t/T) over the K cached logits of each row.
+
+    Teacher distribution over its cached top-K only (blog "Two systems changes",
+    dense-KL bullet: the teacher grid comes from the cached top-K logits).
+    """
+    b = np.asarray(t_rows, dtype=np.float64) / T
+    return b - logsumexp_rows(b)[:, None]
+
+
+def student_logits(H_rows: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """Z = H W^T, the student's output-head logits (one row per position)."""
+    return np.asarray(H_rows, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T
+
+
+def dense_teacher_grid(idx_rows: np.ndarray, logp_rows: np.ndarray, V: int) -> np.ndarray:
+    """p~[n, j] = sum of p_k over the cached entries k of row n with idx_k = j.
+
+    The dense teacher-probability grid of the dense-KL bullet; zero outside
+    the cached ids. Used by the backward for the teacher term of dZ.
+    """
+    n = idx_rows.shape[0]
+    grid = np.zeros((n, V), dtype=np.float64)
+    rows = np.repeat(np.arange(n), idx_rows.shape[1])
+    np.add.at(grid, (rows, idx_rows.reshape(-1).astype(np.int64)), np.exp(logp_rows).reshape(-1))
+    return grid
+
+
+def _blocks(n: int, row_chunk: int):
+    step = max(1, int(row_chunk))
+    for r0 in range(0, n, step):
+        yield r0, min(n, r0 + step)
+
+
+def kd_forward(H, W, idx, t, mask, T: float, row_chunk: int = 64):
+    """Per-row KL(teacher_topK || student) and logsumexp of Z/T.
+
+    For each row n (fp64, exact bf16 values of H and W):
+      a = (H[n] W^T)/T,   lse_n = logsumexp(a),   log q = a - lse_n
+      P = dense teacher grid of row n (softmax of t[n]/T placed at idx[n])
+      loss_n = sum_{j: P_j > 0} P_j (log P_j - log q_j)      if mask_n
+             = 0                                              otherwise
+    This is the dense-KL bullet's computation (blog "Two systems changes"),
+    the pages' correctness baseline. lse is returned for every row (it does
+    not depend on the teacher).
+    Returns (loss[N], lse[N], n_valid).
+    """
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    idx = np.asarray(idx)
+    t = np.asarray(t)
+    mask = np.asarray(mask).astype(bool)
+    N = H.shape[0]
+    loss = np.zeros(N, dtype=np.float64)
+    lse = np.zeros(N, dtype=np.float64)
+    for r0, r1 in _blocks(N, row_chunk):
+        a = student_logits(H[r0:r1], W) / T
+        lse[r0:r1] = logsumexp_rows(a)
+        valid = np.nonzero(mask[r0:r1])[0]
+        if valid.size == 0:
+            continue
+        logp = teacher_log_probs(t[r0:r1][valid], T)
+        P = dense_teacher_grid(idx[r0:r1][valid].astype(np.int64), logp, W.shape[0])
+        log_q = a[valid] - lse[r0:r1][valid][:, None]
+        pos = P > 0
+        terms = np.zeros_like(P)
+        terms[pos] = P[pos] * (np.log(P[pos]) - log_q[pos])
+        loss[r0 + valid] = np.sum(terms, axis=1)
+    return loss, lse, int(mask.sum())
+
+
+def mean_loss(loss: np.ndarray, n_valid: int) -> float:
+    """Mean of the per-row loss over counted rows (0 when nothing is counted)."""
+    return float(np.sum(np.asarray(loss, dtype=np.float64)) / n_valid) if n_valid > 0 else 0.0
+
+
+def kd_backward(H, W, idx, t, mask, T: float, g, row_chunk: int = 64):
+    """Gradients of sum_n g_n * loss_n with respect to H and W.
+
+    With q = softmax(Z/T) over the full vocabulary and p~ the dense teacher grid,
+      dZ[n, j] = (g_n / T) * (q[n, j] - p~[n, j])   (0 on masked rows)
+      dH = dZ W,   dW = dZ^T H
+    (blog "Two systems changes", fused chunked bullet: the backward recomputes
+    each chunk's logits rather than storing them). Returns (dH[N,D], dW[V,D]).
+    """
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    idx = np.asarray(idx)
+    t = np.asarray(t)
+    mask = np.asarray(mask).astype(bool)
+    g = np.asarray(g, dtype=np.float64)
+    N, D = H.shape
+    V = W.shape[0]
+    dH = np.zeros((N, D), dtype=np.float64)
+    dW = np.zeros((V, D), dtype=np.float64)
+    for r0, r1 in _blocks(N, row_chunk):
+        valid = np.nonzero(mask[r0:r1])[0]
+        if valid.size == 0:
+            continue
+        rows = r0 + valid
+        a = student_logits(H[rows], W) / T
+        q = np.exp(a - logsumexp_rows(a)[:, None])
+        ptil = dense_teacher_grid(idx[rows].astype(np.int64), teacher_log_probs(t[rows], T), V)
+        dZ = (g[rows] / T)[:, None] * (q - ptil)
+        dH[rows] = dZ @ W
+        dW += dZ.T @ H[rows]
+    return dH, dW
