@@ -1,0 +1,119 @@
+/*
+ * kd_topk_kl.h — C ABI of the fused top-K KL distillation head (B300, sm_103a).
+ *
+ * What it computes (Efficient Knowledge Distillation for LLMs: Offline Top-K
+ * Logits and a Fused Chunked KL Loss — abstract, and the blog post "Making
+ * Knowledge Distillation Cheap Enough to Run at Scale", section "Two systems
+ * changes"): the student's output projection Z = H W^T is fused into the
+ * KL-divergence loss against a cached teacher top-K, so that no tokens x
+ * vocabulary tensor is ever written to memory. The forward projects the
+ * hidden states tile by tile and folds each tile into a running logsumexp and
+ * a gather of the logits at the teacher's cached ids; the backward recomputes
+ * each chunk of logits instead of storing them.
+ *
+ * Per counted row n (mask[n] = 1), with temperature T > 0:
+ *   q    = softmax(Z[n] / T) over all V tokens            (student)
+ *   P    = softmax(t[n] / T) placed at idx[n], 0 elsewhere (teacher grid;
+ *          a repeated id gets the sum of its entries)
+ *   loss = sum_j P_j (log P_j - log q_j)
+ *   lse  = logsumexp(Z[n] / T)                             (natural log)
+ * A masked row gets loss 0 and zero gradient, and its idx/t are never read.
+ * The mean loss is sum(loss) / n_valid, formed by the caller.
+ *
+ * Conventions shared by every call:
+ *   - All pointers are DEVICE pointers owned by the caller. The library never
+ *     allocates, frees or synchronises (kd_get_status is the one exception:
+ *     it synchronises the given stream).
+ *   - Every compute call is asynchronous on `stream` (a cudaStream_t; 0 is the
+ *     legacy default stream).
+ *   - Layouts are row-major and contiguous. bf16 tensors are passed as
+ *     uint16_t bit patterns.
+ *   - H, W, dH and the workspace must be 16-byte aligned; the other arrays
+ *     4-byte aligned (mask 1-byte). D must be a multiple of 8, 1 <= K <= 256,
+ *     V >= 1, T finite and > 0.
+ *   - Argument errors are returned synchronously and nothing is launched.
+ *     Errors found on the device (an id outside [0, V) at a counted row, a
+ *     bounded wait that ran out) are recorded in a per-device status word and
+ *     returned by kd_get_status.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef KD_TOPK_KL_H
+#define KD_TOPK_KL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KD_OK = 0,
+  KD_ERR_ARG = 1,          /* bad size, NULL pointer or bad T */
+  KD_ERR_ALIGN = 2,        /* a pointer breaks the alignment rules above */
+  KD_ERR_UNSUPPORTED = 3,  /* shape outside what the kernels handle, or no sm_103 device */
+  KD_ERR_WORKSPACE = 4,    /* ws_bytes smaller than kd_topk_kl_workspace_size() */
+  KD_ERR_INDEX = 5,        /* device: a teacher id outside [0, V) at a counted row */
+  KD_ERR_TIMEOUT = 6,      /* device: a bounded pipeline wait ran out; results invalid */
+  KD_ERR_CUDA = 7          /* a CUDA runtime/driver call failed */
+} kd_status;
+
+/* Opaque stream handle; pass a cudaStream_t. */
+typedef struct CUstream_st* kd_stream_t;
+
+/*
+ * Bytes of device workspace that kd_topk_kl_fwd and kd_topk_kl_bwd need for
+ * these sizes (one buffer serves both calls). The only vocabulary-sized part
+ * is one chunk of dZ (chunk_tokens x V bf16), so the size grows linearly in N
+ * and never as N x V. chunk_tokens is the backward's row-chunk C (rounded up
+ * to a multiple of 128 internally; <= 0 selects 4096). Returns 0 for invalid
+ * sizes. Pure host arithmetic; safe without a GPU.
+ */
+size_t kd_topk_kl_workspace_size(int64_t N, int D, int V, int K, int64_t chunk_tokens);
+
+/*
+ * Forward. Inputs: H [N x D] bf16 (final hidden states), W [V x D] bf16
+ * (lm-head weight), topk_idx [N x K] int32 teacher ids, topk_logit [N x K]
+ * fp32 teacher logits, mask [N] uint8 (NULL = every row counted).
+ * Outputs: loss [N] fp32 per-row KL (0 at masked rows), lse [N] fp32
+ * logsumexp of Z/T for every row, n_valid [1] int64 count of counted rows.
+ * ws: workspace of at least kd_topk_kl_workspace_size(N, D, V, K, 0) bytes;
+ * its contents on entry do not matter and are clobbered.
+ */
+kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                         const float* topk_logit, const uint8_t* mask, int64_t N, int D, int V,
+                         int K, float T, float* loss, float* lse, int64_t* n_valid, void* ws,
+                         size_t ws_bytes, kd_stream_t stream);
+
+/*
+ * Backward of L = sum_n dloss[n] * loss[n]. Takes the forward's inputs plus
+ * lse [N] from kd_topk_kl_fwd and dloss [N] fp32 (for the mean loss:
+ * 1/n_valid at counted rows). Recomputes the logits chunk by chunk
+ * (chunk_tokens rows at a time; the result does not depend on it) and writes
+ *   dH [N x D] bf16  = dZ W
+ *   dW [V x D] fp32  = dZ^T H   (added to the existing dW if accumulate_dW != 0,
+ *                                 overwritten otherwise)
+ * with dZ = (dloss/T) (q - P) at counted rows and 0 elsewhere.
+ * ws: at least kd_topk_kl_workspace_size(N, D, V, K, chunk_tokens) bytes.
+ */
+kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                         const float* topk_logit, const uint8_t* mask, const float* lse,
+                         const float* dloss, int64_t N, int D, int V, int K, float T,
+                         int64_t chunk_tokens, int accumulate_dW, uint16_t* dH, float* dW,
+                         void* ws, size_t ws_bytes, kd_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word (KD_OK, KD_ERR_INDEX or KD_ERR_TIMEOUT), or KD_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+kd_status kd_get_status(kd_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* kd_status_string(kd_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KD_TOPK_KL_H */

@@ -1,0 +1,56 @@
+/*
+ * kd_topk_kl_testing.h — test hooks of libkdtopk. Not part of the loss API.
+ *
+ * They expose the pieces the loss is built from so that tests can check each
+ * one on its own: the tcgen05 GEMM mainloop as a plain GEMM, the work
+ * schedule as host arithmetic, and the bounded-wait error path.
+ * Ownership, stream and error rules are those of kd_topk_kl.h.
+ */
+#ifndef KD_TOPK_KL_TESTING_H
+#define KD_TOPK_KL_TESTING_H
+
+#include "kd_topk_kl.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * C[m][n] = sum_k A(m,k) * B(n,k) in fp32 through the same persistent
+ * tcgen05/TMA mainloop the loss kernels use (bf16 operands, fp32 accumulate).
+ * a_mn = 0: A is [M x K] row-major (K contiguous); a_mn = 1: A is [K x M]
+ * row-major (M contiguous). b_mn likewise for B ([N x K] or [K x N]).
+ * C is [M x N] fp32 row-major. Device pointers, 16-byte aligned; M, N and K
+ * must be multiples of 8. (a_mn, b_mn) = (1, 0) is not supported.
+ */
+kd_status kd_debug_gemm_bf16(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K,
+                             int a_mn, int b_mn, kd_stream_t stream);
+
+/*
+ * Launches one block whose pipeline wait can never be satisfied (nothing
+ * arrives on its barrier). The wait gives up after timeout_ns nanoseconds
+ * (capped at 2 s), records KD_ERR_TIMEOUT in the status word and the kernel
+ * returns normally. Read the result with kd_get_status.
+ */
+kd_status kd_debug_wait_timeout(uint64_t timeout_ns, kd_stream_t stream);
+
+/*
+ * Host-side description of the work schedule the library would use.
+ * kind: 0 = forward / dZ recompute (rows x vocabulary tiles),
+ *       1 = dH (tokens x hidden tiles, split over the vocabulary),
+ *       2 = dW (vocabulary x hidden tiles).
+ * rows, cols, depth: the GEMM's M, N (columns) and K extents; num_sms: the
+ * SM count to plan for. counts (optional, length MB*NB*KBLOCKS, where MB =
+ * ceil(rows/128), NB = number of column tiles, KBLOCKS = ceil(depth/64)) is
+ * incremented once per (m-tile, n-tile, k-block) the schedule visits.
+ * info (length 8) receives {units, grid, MB, NB, KBLOCKS, BN, max_slots,
+ * k_splits}. Returns KD_ERR_ARG for bad sizes.
+ */
+kd_status kd_debug_schedule(int kind, int64_t rows, int64_t cols, int64_t depth, int num_sms,
+                            int32_t* counts, int64_t* info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KD_TOPK_KL_TESTING_H */

@@ -1,0 +1,33 @@
+"""The tcgen05/TMA mainloop on its own, as a plain GEMM against torch.matmul in
+fp32 on the same bf16 operands, for the three operand layouts the loss uses:
+both K-major (logits), B MN-major (dH = dZ W) and both MN-major (dW = dZ^T H).
+"""
+import pytest
+import torch
+
+from top_kl_loss_lm_b300 import binding
+
+pytestmark = pytest.mark.gpu
+
+
+def _ref(A, B, a_mn, b_mn):
+    Af = A.float().T if a_mn else A.float()
+    Bf = B.float() if b_mn else B.float().T
+    return Af @ Bf
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, True)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 128), (200, 264, 136),
+                                   (128, 240, 64), (1024, 2880, 1024), (384, 1000, 8)])
+def test_gemm_matches_torch(a_mn, b_mn, M, N, K):
+    g = torch.Generator(device="cuda").manual_seed(M * 7 + N * 3 + K)
+    A = torch.randn((K, M) if a_mn else (M, K), device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn((K, N) if b_mn else (N, K), device="cuda", generator=g).to(torch.bfloat16)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    binding.kd_debug_gemm_bf16(A, B, C, a_mn, b_mn)
+    torch.cuda.synchronize()
+    assert binding.kd_get_status() == 0
+    R = _ref(A, B, a_mn, b_mn)
+    assert torch.isfinite(C).all()
+    err = (C - R).abs().max().item() / R.abs().max().item()
+    assert err < 1e-4, err

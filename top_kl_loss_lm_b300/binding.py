@@ -1,0 +1,192 @@
+"""ctypes binding of libkdtopk (include/kd_topk_kl.h), same names as the C ABI.
+
+This layer only marshals: it checks dtypes, shapes and devices of torch
+tensors, passes their data pointers and the current CUDA stream, and turns a
+non-zero kd_status into ``KdError``. Every step of the loss runs in the CUDA
+library; there is no fallback. If ``libkdtopk.so`` is missing the first call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "KdError", "lib", "library_path",
+    "kd_topk_kl_workspace_size", "kd_topk_kl_fwd", "kd_topk_kl_bwd",
+    "kd_get_status", "kd_status_string",
+    "kd_debug_gemm_bf16", "kd_debug_wait_timeout", "kd_debug_schedule",
+    "STATUS",
+]
+
+STATUS = {
+    0: "KD_OK", 1: "KD_ERR_ARG", 2: "KD_ERR_ALIGN", 3: "KD_ERR_UNSUPPORTED",
+    4: "KD_ERR_WORKSPACE", 5: "KD_ERR_INDEX", 6: "KD_ERR_TIMEOUT", 7: "KD_ERR_CUDA",
+}
+
+_LIB = None
+_LOCK = threading.Lock()
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkdtopk.so")
+
+
+class KdError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {STATUS.get(self.code, self.code)} ({kd_status_string(self.code)})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkdtopk.so (once) and declare its signatures."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    with _LOCK:
+        if _LIB is not None:
+            return _LIB
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -m top_kl_loss_lm_b300.build`")
+        L = ctypes.CDLL(path)
+        vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.kd_topk_kl_workspace_size.argtypes = [i64, i32, i32, i32, i64]
+        L.kd_topk_kl_workspace_size.restype = sz
+        L.kd_topk_kl_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp, vp, sz, vp]
+        L.kd_topk_kl_fwd.restype = i32
+        L.kd_topk_kl_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, i64, i32,
+                                     vp, vp, vp, sz, vp]
+        L.kd_topk_kl_bwd.restype = i32
+        L.kd_get_status.argtypes = [vp]
+        L.kd_get_status.restype = i32
+        L.kd_status_string.argtypes = [i32]
+        L.kd_status_string.restype = ctypes.c_char_p
+        L.kd_debug_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp]
+        L.kd_debug_gemm_bf16.restype = i32
+        L.kd_debug_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.kd_debug_wait_timeout.restype = i32
+        L.kd_debug_schedule.argtypes = [i32, i64, i64, i64, i32, vp, vp]
+        L.kd_debug_schedule.restype = i32
+        _LIB = L
+        return L
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype, shape, name: str, device=None):
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if not t.is_cuda or (device is not None and t.device != device):
+        raise ValueError(f"{name}: must be on {device or 'a CUDA device'}")
+    return t.data_ptr()
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise KdError(code, where)
+
+
+def kd_status_string(code: int) -> str:
+    return lib().kd_status_string(int(code)).decode()
+
+
+def kd_topk_kl_workspace_size(N: int, D: int, V: int, K: int, chunk_tokens: int = 0) -> int:
+    return int(lib().kd_topk_kl_workspace_size(N, D, V, K, chunk_tokens))
+
+
+def kd_topk_kl_fwd(H, W, topk_idx, topk_logit, mask, T: float, loss, lse, n_valid, ws, stream=None):
+    """Forward into caller-owned tensors (see kd_topk_kl_fwd in the header)."""
+    N, D = H.shape
+    V = W.shape[0]
+    K = topk_idx.shape[1]
+    dev = H.device
+    args = (
+        _ptr(H, torch.bfloat16, (N, D), "H", dev), _ptr(W, torch.bfloat16, (V, D), "W", dev),
+        _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
+        _ptr(topk_logit, torch.float32, (N, K), "topk_logit", dev),
+        _ptr(mask, torch.uint8, (N,), "mask", dev),
+        N, D, V, K, float(T),
+        _ptr(loss, torch.float32, (N,), "loss", dev), _ptr(lse, torch.float32, (N,), "lse", dev),
+        _ptr(n_valid, torch.int64, (1,), "n_valid", dev),
+        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream),
+    )
+    _check(lib().kd_topk_kl_fwd(*args), "kd_topk_kl_fwd")
+
+
+def kd_topk_kl_bwd(H, W, topk_idx, topk_logit, mask, lse, dloss, T: float, chunk_tokens: int,
+                   accumulate_dW: bool, dH, dW, ws, stream=None):
+    """Backward into caller-owned dH (bf16) and dW (fp32)."""
+    N, D = H.shape
+    V = W.shape[0]
+    K = topk_idx.shape[1]
+    dev = H.device
+    args = (
+        _ptr(H, torch.bfloat16, (N, D), "H", dev), _ptr(W, torch.bfloat16, (V, D), "W", dev),
+        _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
+        _ptr(topk_logit, torch.float32, (N, K), "topk_logit", dev),
+        _ptr(mask, torch.uint8, (N,), "mask", dev),
+        _ptr(lse, torch.float32, (N,), "lse", dev), _ptr(dloss, torch.float32, (N,), "dloss", dev),
+        N, D, V, K, float(T), int(chunk_tokens), 1 if accumulate_dW else 0,
+        _ptr(dH, torch.bfloat16, (N, D), "dH", dev), _ptr(dW, torch.float32, (V, D), "dW", dev),
+        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream),
+    )
+    _check(lib().kd_topk_kl_bwd(*args), "kd_topk_kl_bwd")
+
+
+def kd_get_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(lib().kd_get_status(_stream(stream)))
+
+
+def kd_debug_gemm_bf16(A, B, C, a_mn: bool, b_mn: bool, stream=None):
+    """C = A·B^T through the tcgen05 mainloop (see kd_topk_kl_testing.h)."""
+    if a_mn:
+        K, M = A.shape
+    else:
+        M, K = A.shape
+    N = B.shape[1] if b_mn else B.shape[0]
+    dev = A.device
+    _ptr(A, torch.bfloat16, tuple(A.shape), "A", dev)
+    _ptr(B, torch.bfloat16, tuple(B.shape), "B", dev)
+    _ptr(C, torch.float32, (M, N), "C", dev)
+    _check(lib().kd_debug_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                    int(a_mn), int(b_mn), _stream(stream)), "kd_debug_gemm_bf16")
+
+
+def kd_debug_wait_timeout(timeout_ns: int, stream=None):
+    _check(lib().kd_debug_wait_timeout(int(timeout_ns), _stream(stream)), "kd_debug_wait_timeout")
+
+
+def kd_debug_schedule(kind: int, rows: int, cols: int, depth: int, num_sms: int, with_counts=True):
+    """Host-only: the work schedule as (info dict, per-(m, n, k-block) visit counts or None)."""
+    import numpy as np
+    info = np.zeros(8, dtype=np.int64)
+    code = lib().kd_debug_schedule(kind, rows, cols, depth, num_sms, None, info.ctypes.data)
+    _check(code, "kd_debug_schedule")
+    counts = None
+    if with_counts:
+        MB, NB, KB = int(info[2]), int(info[3]), int(info[4])
+        counts = np.zeros(MB * NB * KB, dtype=np.int32)
+        info2 = np.zeros(8, dtype=np.int64)
+        _check(lib().kd_debug_schedule(kind, rows, cols, depth, num_sms, counts.ctypes.data,
+                                       info2.ctypes.data), "kd_debug_schedule")
+        counts = counts.reshape(MB, NB, KB)
+    keys = ["units", "grid", "MB", "NB", "KB", "BN", "max_slots", "k_splits"]
+    return {k: int(v) for k, v in zip(keys, info)}, counts

@@ -1,0 +1,440 @@
+// kd_gemm.cuh — persistent, warp-specialised tcgen05 GEMM for sm_103a with the
+// loss epilogues fused in.
+//
+//   warp 0      TMA producer: fills a STAGES-deep ring of (A, B) k-blocks
+//   warp 1      TMEM owner + MMA issuer: 128 x BN x 16 bf16 MMAs into one of two
+//               fp32 TMEM accumulators (2 x 256 columns), so the epilogue of one
+//               tile overlaps the main loop of the next
+//   warps 2..5  epilogue: each thread owns one accumulator row (TMEM lane)
+//
+// Epilogues:
+//   kEpiFwd   online max / sum-of-exp of Z/T over the unit's vocabulary tiles
+//             (partial per row and split) + gather of Z at the row's sorted
+//             teacher ids that fall in the tile
+//   kEpiDz    dZ = (g/T)(exp(Z/T - lse) - P~) with P~ scattered from the sorted
+//             ids, rounded to bf16 into the chunk's dZ buffer
+//   kEpiDh    dH tile (bf16, or fp32 partial per k-split)
+//   kEpiDw    dW tile, stored or added to the existing fp32 values
+//   kEpiPlain fp32 C tile (mainloop test hook)
+//
+// Operand layouts in shared memory are the TMA 128-byte-swizzled boxes: a
+// K-major operand is rows x 64 bf16 (one 128-byte line per row); an MN-major
+// operand is 64-wide MN slabs of 64 k-rows, 8 KB each.
+#pragma once
+
+#include <climits>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "kd_ptx.cuh"
+#include "kd_sched.h"
+
+namespace kd {
+
+constexpr int kStages = 4;
+constexpr int kAStageBytes = kBM * kBK * 2;      // 16 KB
+constexpr int kBStageBytes = kBNMax * kBK * 2;   // 32 KB
+constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+constexpr int kSlabBytes = 64 * kBK * 2;         // one 64-wide MN slab of a k-block: 8 KB
+constexpr int kGemmThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+enum Epi : int { kEpiFwd = 0, kEpiDz = 1, kEpiDh = 2, kEpiDw = 3, kEpiPlain = 4 };
+
+struct GemmArgs {
+  Sched sched;
+  int M;              // valid output rows (fwd: N, dz/dh: rows in chunk, dw: V, plain: M)
+  int Ncols;          // valid output columns (fwd/dz: V, dh/dw: D, plain: N)
+  int BN;             // tile width = MMA N (multiple of 16, <= 256)
+  uint32_t idesc;
+  int a_row_off;      // K-major A: row offset added to the tile row (chunk start in H)
+  int b_k_off;        // MN-major B: k-row offset (chunk start in H for dW)
+  int64_t row_base;   // global token of local row 0 (dz, dh)
+  int K;              // teacher top-K
+  float scale2;       // log2(e) / T
+  float inv_T;
+  const int2* pairs;  // N x K sorted (id, p bits)
+  float* zk;          // N x K gathered logits (sorted order)
+  float2* part;       // N x slots (max, sum) in base-2 units
+  int slots;
+  const float* lse;
+  const float* dloss;
+  const uint8_t* mask;
+  uint16_t* dz;       // chunk dZ buffer, row stride dz_ld
+  int64_t dz_ld;
+  float* out_f32;     // dh partials / dW / plain C
+  int64_t ld_out;
+  int64_t part_stride;  // dh: elements per k-split slice
+  uint16_t* out_bf16;   // dH
+  int accumulate;       // dW: add to existing values
+  int* status;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ float select32(const float (&v)[32], int j) {
+  float r = v[0];
+#pragma unroll
+  for (int i = 1; i < 32; ++i) r = (j == i) ? v[i] : r;
+  return r;
+}
+
+__device__ __forceinline__ void sub_at32(float (&v)[32], int j, float x) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = (j == i) ? v[i] - x : v[i];
+}
+
+__device__ __forceinline__ int lower_bound_id(const int2* p, int K, int target) {
+  int lo = 0, hi = K;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(&p[mid].x) < target)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Store 8 fp32 (32 bytes) or add them to what is there.
+__device__ __forceinline__ void store8_f32(float* dst, const float* v, bool add) {
+  float4 a = make_float4(v[0], v[1], v[2], v[3]);
+  float4 b = make_float4(v[4], v[5], v[6], v[7]);
+  if (add) {
+    const float4 oa = *reinterpret_cast<const float4*>(dst);
+    const float4 ob = *reinterpret_cast<const float4*>(dst + 4);
+    a.x += oa.x; a.y += oa.y; a.z += oa.z; a.w += oa.w;
+    b.x += ob.x; b.y += ob.y; b.z += ob.z; b.w += ob.w;
+  }
+  *reinterpret_cast<float4*>(dst) = a;
+  *reinterpret_cast<float4*>(dst + 4) = b;
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* acc_full = empty_bar + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain_bar = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Sched& sc = args.sched;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);  // one arrive per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0;         // stages loaded at least once
+      uint32_t last_parity = 0;         // parity of each stage's last load
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < sc.total; u += gridDim.x) {
+        const Unit d = sched_unit(sc, u);
+        const int m0 = d.m_blk * kBM;
+        for (int nb = d.n_begin; ok && nb < d.n_end; ++nb) {
+          const int n0 = nb * args.BN;
+          for (int kb = d.kb_begin; kb < d.kb_end; ++kb) {
+            if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, args.timeout_ns,
+                                   args.status, 6)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+            uint8_t* a_dst = smem + stage * kStageBytes;
+            uint8_t* b_dst = a_dst + kAStageBytes;
+            const int k0 = kb * kBK;
+            if (!A_MN) {
+              tma_load_2d(a_dst, &tmA, &full_bar[stage], k0, m0 + args.a_row_off);
+            } else {
+              tma_load_2d(a_dst, &tmA, &full_bar[stage], m0, k0);
+              tma_load_2d(a_dst + kSlabBytes, &tmA, &full_bar[stage], m0 + 64, k0);
+            }
+            if (!B_MN) {
+              tma_load_2d(b_dst, &tmB, &full_bar[stage], k0, n0);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                tma_load_2d(b_dst + j * kSlabBytes, &tmB, &full_bar[stage], n0 + 64 * j,
+                            k0 + args.b_k_off);
+            }
+            issued_mask |= 1u << stage;
+            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Leave no bulk copy in flight into this CTA's shared memory.
+        for (int s = 0; s < kStages; ++s)
+          if (issued_mask & (1u << s)) {
+            volatile int no_abort = 0;
+            mbar_wait_bounded(&full_bar[s], (last_parity >> s) & 1u, &no_abort, 100000000ull,
+                              args.status, 6);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool any_mma = false;
+      const uint32_t a_lbo = A_MN ? kSlabBytes : 16;
+      const uint32_t b_lbo = B_MN ? kSlabBytes : 16;
+      const uint32_t a_kstep = A_MN ? 16 * 128 : 32;  // bytes per 16-wide k step
+      const uint32_t b_kstep = B_MN ? 16 * 128 : 32;
+      for (int64_t u = blockIdx.x; ok && u < sc.total; u += gridDim.x) {
+        const Unit d = sched_unit(sc, u);
+        for (int nb = d.n_begin; ok && nb < d.n_end; ++nb) {
+          if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, args.timeout_ns,
+                                 args.status, 6)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBNMax);
+          for (int kb = d.kb_begin; kb < d.kb_end; ++kb) {
+            if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, args.timeout_ns,
+                                   args.status, 6)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
+            const uint32_t b_addr = a_addr + kAStageBytes;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t adesc = umma_smem_desc(a_addr + k * a_kstep, a_lbo, 1024);
+              const uint64_t bdesc = umma_smem_desc(b_addr + k * b_kstep, b_lbo, 1024);
+              umma_bf16(d_tmem, adesc, bdesc, args.idesc,
+                        (kb > d.kb_begin || k > 0) ? 1u : 0u);
+            }
+            any_mma = true;
+            umma_commit(&empty_bar[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&acc_full[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && any_mma) {
+        // Let every issued MMA finish before TMEM is released.
+        umma_commit(drain_bar);
+        volatile int no_abort = 0;
+        mbar_wait_bounded(drain_bar, 0, &no_abort, 100000000ull, args.status, 6);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM sub-partition this warp may read
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    const int K = args.K;
+    for (int64_t u = blockIdx.x; ok && u < sc.total; u += gridDim.x) {
+      const Unit d = sched_unit(sc, u);
+      const int m0 = d.m_blk * kBM;
+      const int row = m0 + row_in_tile;          // local output row
+      const bool row_ok = row < args.M;
+      // per-unit state
+      float m2 = -INFINITY, s2 = 0.0f;           // fwd running (max, sum) in base 2
+      int ptr = 0;
+      int2 cur = make_int2(INT_MAX, 0);          // current entry of the sorted teacher list
+      int64_t rowK = 0;
+      float gs = 0.0f, lse2 = 0.0f;
+      bool dz_row = false;
+      if (EPI == kEpiFwd && row_ok) {
+        rowK = static_cast<int64_t>(row) * K;
+        ptr = lower_bound_id(args.pairs + rowK, K, d.n_begin * args.BN);
+        cur.x = (ptr < K) ? __ldg(&args.pairs[rowK + ptr].x) : INT_MAX;
+      }
+      if (EPI == kEpiDz && row_ok) {
+        const int64_t g = args.row_base + row;
+        dz_row = (args.mask == nullptr) || (args.mask[g] != 0);
+        if (dz_row) {
+          gs = __ldg(&args.dloss[g]) * args.inv_T;
+          lse2 = __ldg(&args.lse[g]) * 1.4426950408889634f;
+          rowK = g * K;
+          ptr = lower_bound_id(args.pairs + rowK, K, d.n_begin * args.BN);
+          cur = (ptr < K) ? __ldg(&args.pairs[rowK + ptr]) : make_int2(INT_MAX, 0);
+        }
+      }
+      for (int nb = d.n_begin; nb < d.n_end; ++nb) {
+        const bool got = mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag, args.timeout_ns,
+                                           args.status, 6);
+        if (!__all_sync(0xffffffffu, got)) {  // keep the warp's decision uniform
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tacc = lane_addr + static_cast<uint32_t>(acc * kBNMax);
+        const int col_tile = nb * args.BN;
+#pragma unroll 1
+        for (int c = 0; c < kBNMax / 32; ++c) {
+          if (32 * c >= args.BN) break;
+          const int col0 = col_tile + 32 * c;
+          if (col0 >= args.Ncols && EPI != kEpiDz) break;
+          float v[32];
+          __syncwarp();
+          tmem_ld32(tacc + 32 * c, v);
+          if constexpr (EPI == kEpiFwd) {
+            while (cur.x < col0 + 32) {
+              args.zk[rowK + ptr] = select32(v, cur.x - col0);
+              ++ptr;
+              cur.x = (ptr < K) ? __ldg(&args.pairs[rowK + ptr].x) : INT_MAX;
+            }
+            if (col0 + 32 > args.Ncols) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col0 + i >= args.Ncols) v[i] = -INFINITY;
+            }
+            float mx = v[0];
+#pragma unroll
+            for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
+            const float mnew = fmaxf(m2, mx * args.scale2);
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              a0 += ex2_approx(fmaf(v[i + 0], args.scale2, -mnew));
+              a1 += ex2_approx(fmaf(v[i + 1], args.scale2, -mnew));
+              a2 += ex2_approx(fmaf(v[i + 2], args.scale2, -mnew));
+              a3 += ex2_approx(fmaf(v[i + 3], args.scale2, -mnew));
+            }
+            s2 = s2 * ex2_approx(m2 - mnew) + ((a0 + a1) + (a2 + a3));
+            m2 = mnew;
+          } else if constexpr (EPI == kEpiDz) {
+            float dv[32];
+            if (dz_row) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) dv[i] = gs * ex2_approx(fmaf(v[i], args.scale2, -lse2));
+              while (cur.x < col0 + 32) {
+                sub_at32(dv, cur.x - col0, gs * __int_as_float(cur.y));
+                ++ptr;
+                cur = (ptr < K) ? __ldg(&args.pairs[rowK + ptr]) : make_int2(INT_MAX, 0);
+              }
+              if (col0 + 32 > args.Ncols) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col0 + i >= args.Ncols) dv[i] = 0.0f;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) dv[i] = 0.0f;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(args.dz + static_cast<int64_t>(row) * args.dz_ld + col0);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              uint4 w;
+              w.x = pack_bf16x2(dv[8 * g + 0], dv[8 * g + 1]);
+              w.y = pack_bf16x2(dv[8 * g + 2], dv[8 * g + 3]);
+              w.z = pack_bf16x2(dv[8 * g + 4], dv[8 * g + 5]);
+              w.w = pack_bf16x2(dv[8 * g + 6], dv[8 * g + 7]);
+              dst[g] = w;
+            }
+          } else if constexpr (EPI == kEpiDh) {
+            if (row_ok) {
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                const int cg = col0 + 8 * g;
+                if (32 * c + 8 * g < args.BN && cg < args.Ncols) {
+                  if (args.sched.KS == 1) {
+                    uint4 w;
+                    w.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
+                    w.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
+                    w.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
+                    w.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
+                    *reinterpret_cast<uint4*>(args.out_bf16 + (args.row_base + row) * args.Ncols + cg) = w;
+                  } else {
+                    store8_f32(args.out_f32 + d.slot * args.part_stride +
+                                   static_cast<int64_t>(row) * args.Ncols + cg,
+                               &v[8 * g], false);
+                  }
+                }
+              }
+            }
+          } else {  // kEpiDw, kEpiPlain
+            if (row_ok) {
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                const int cg = col0 + 8 * g;
+                if (32 * c + 8 * g < args.BN && cg < args.Ncols)
+                  store8_f32(args.out_f32 + static_cast<int64_t>(row) * args.ld_out + cg, &v[8 * g],
+                             EPI == kEpiDw && args.accumulate != 0);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (EPI == kEpiFwd && ok && row_ok)
+        args.part[static_cast<int64_t>(row) * args.slots + d.slot] = make_float2(m2, s2);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+}  // namespace kd

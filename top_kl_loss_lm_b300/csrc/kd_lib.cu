@@ -1,0 +1,503 @@
+// kd_lib.cu — host side of libkdtopk: argument checks, workspace plan, TMA
+// descriptors, and the launch sequence of the forward and backward.
+//
+// Forward  (one pass over the vocabulary, nothing tokens x vocabulary stored):
+//   prep -> fused GEMM + online logsumexp + top-K gather -> combine
+// Backward (the logits are recomputed, C tokens at a time):
+//   prep -> for each chunk: GEMM + dZ epilogue (dZ chunk, bf16)
+//                           -> dH = dZ W  (split over V, fixed-order sum)
+//                           -> dW (+)= dZ^T H
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/kd_topk_kl.h"
+#include "../../include/kd_topk_kl_testing.h"
+#include "kd_aux.cuh"
+#include "kd_gemm.cuh"
+#include "kd_sched.h"
+
+namespace kd {
+
+__device__ int g_kd_status;  // first device-side error since the last kd_get_status
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+  bool ready = false;
+  bool ok = false;
+  int num_sms = 0;
+  int* status = nullptr;  // device address of g_kd_status
+};
+
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+const DevInfo* device_info(kd_status* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    *err = KD_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.ready) {
+    d.ready = true;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    void* p = nullptr;
+    const bool sym = cudaGetSymbolAddress(&p, g_kd_status) == cudaSuccess;
+    d.status = static_cast<int*>(p);
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) == cudaSuccess &&
+          q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ok = sym && g_encode != nullptr && major == 10 && minor == 3 && d.num_sms > 0;
+    cudaGetLastError();
+  }
+  if (!d.ok) {
+    *err = KD_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  return &d;
+}
+
+// 2D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// `row_bytes` between rows, box of box_inner x box_outer, 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+              uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  std::memset(m, 0, sizeof(*m));
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Layout {
+  // shared by forward and backward
+  size_t pairs = 0, ent = 0;
+  // forward
+  size_t part = 0, zk = 0;
+  // backward
+  size_t dz = 0, dhp = 0;
+  size_t fwd_end = 0, bwd_end = 0, total = 0;
+  int slots = 0;
+  int64_t C = 0, C_pad = 0, dz_ld = 0;
+  int NB = 0;
+};
+
+Layout plan(int64_t N, int D, int V, int K, int64_t chunk) {
+  Layout L;
+  L.NB = static_cast<int>(cdiv(V, kBNMax));
+  L.slots = L.NB < kMaxSlots ? L.NB : kMaxSlots;
+  size_t off = 0;
+  L.pairs = off;
+  off = align256(off + static_cast<size_t>(N) * K * sizeof(int2));
+  L.ent = off;
+  off = align256(off + static_cast<size_t>(N) * sizeof(float));
+  const size_t common = off;
+  // forward
+  L.part = off;
+  off = align256(off + static_cast<size_t>(N) * L.slots * sizeof(float2));
+  L.zk = off;
+  off = align256(off + static_cast<size_t>(N) * K * sizeof(float));
+  L.fwd_end = off;
+  // backward (reuses the forward's region)
+  off = common;
+  int64_t C = chunk <= 0 ? 4096 : chunk;
+  C = cdiv(C, kBM) * kBM;
+  const int64_t Nr = cdiv(N, kBM) * kBM;
+  if (C > Nr) C = Nr;
+  if (C < kBM) C = kBM;
+  L.C = C;
+  L.C_pad = C;
+  L.dz_ld = static_cast<int64_t>(L.NB) * kBNMax;
+  L.dz = off;
+  off = align256(off + static_cast<size_t>(L.C_pad) * L.dz_ld * sizeof(uint16_t));
+  L.dhp = off;  // k-split partials of dH take whatever follows (sized at call time)
+  L.bwd_end = off;
+  L.total = L.fwd_end > L.bwd_end ? L.fwd_end : L.bwd_end;
+  return L;
+}
+
+// dH partial slices that fit in ws_bytes after the fixed backward layout.
+int ksplit_that_fits(const Layout& L, int D, size_t ws_bytes, int wanted) {
+  if (wanted <= 1) return 1;
+  const size_t slice = static_cast<size_t>(L.C_pad) * D * sizeof(float);
+  if (ws_bytes <= L.dhp) return 1;
+  const size_t room = ws_bytes - L.dhp;
+  int fit = static_cast<int>(room / slice);
+  if (fit < 2) return 1;
+  return fit < wanted ? fit : wanted;
+}
+
+int wanted_ksplit(int64_t C_pad, int D, int V, int num_sms) {
+  const int MB = static_cast<int>(C_pad / kBM);
+  const int bn = hidden_tile_width(D);
+  const int NBd = static_cast<int>(cdiv(D, bn));
+  const int KB = static_cast<int>(cdiv(V, kBK));
+  return choose_ksplit(static_cast<int64_t>(MB) * NBd, KB, num_sms);
+}
+
+kd_status cuda_check() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
+template <int EPI, bool AMN, bool BMN>
+kd_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int num_sms,
+                      cudaStream_t s) {
+  auto kern = kd_gemm_kernel<EPI, AMN, BMN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return KD_ERR_CUDA;
+  }
+  int64_t grid = args.sched.total < num_sms ? args.sched.total : num_sms;
+  if (grid < 1) return KD_OK;
+  kern<<<static_cast<unsigned>(grid), kGemmThreads, kGemmSmemBytes, s>>>(a, b, args);
+  return cuda_check();
+}
+
+GemmArgs base_args(const DevInfo* di) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.status = di->status;
+  a.timeout_ns = 2000000000ull;  // 2 s: far above any stage wait of a healthy pipeline
+  return a;
+}
+
+kd_status check_common(const uint16_t* H, const uint16_t* W, const int32_t* idx, const float* t,
+                       int64_t N, int D, int V, int K, float T, const void* ws) {
+  if (N < 0 || D <= 0 || V <= 0 || K < 1 || K > kMaxTopK) return KD_ERR_ARG;
+  if (D % 8 != 0) return KD_ERR_ARG;
+  if (!(T > 0.0f) || !std::isfinite(T)) return KD_ERR_ARG;
+  if (N > (int64_t(1) << 31) - kBM || V > (1 << 30)) return KD_ERR_UNSUPPORTED;
+  if (N == 0) return KD_OK;
+  if (!H || !W || !idx || !t || !ws) return KD_ERR_ARG;
+  if (!aligned(H, 16) || !aligned(W, 16) || !aligned(ws, 256) || !aligned(idx, 4) || !aligned(t, 4))
+    return KD_ERR_ALIGN;
+  return KD_OK;
+}
+
+}  // namespace
+}  // namespace kd
+
+using namespace kd;
+
+extern "C" size_t kd_topk_kl_workspace_size(int64_t N, int D, int V, int K, int64_t chunk_tokens) {
+  if (N < 0 || D <= 0 || V <= 0 || K < 1 || K > kMaxTopK || D % 8 != 0) return 0;
+  Layout L = plan(N, D, V, K, chunk_tokens);
+  int sms = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) sms = n;
+  }
+  cudaGetLastError();
+  const int ks = wanted_ksplit(L.C_pad, D, V, sms);
+  size_t bwd = L.bwd_end;
+  if (ks > 1) bwd = align256(L.dhp + static_cast<size_t>(ks) * L.C_pad * D * sizeof(float));
+  return L.fwd_end > bwd ? L.fwd_end : bwd;
+}
+
+extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                                    const float* topk_logit, const uint8_t* mask, int64_t N, int D,
+                                    int V, int K, float T, float* loss, float* lse,
+                                    int64_t* n_valid, void* ws, size_t ws_bytes,
+                                    kd_stream_t stream) {
+  kd_status st = check_common(H, W, topk_idx, topk_logit, N, D, V, K, T, ws);
+  if (st != KD_OK) return st;
+  if (!n_valid || (N > 0 && (!loss || !lse))) return KD_ERR_ARG;
+  if (!aligned(n_valid, 8) || !aligned(loss, 4) || !aligned(lse, 4)) return KD_ERR_ALIGN;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s) != cudaSuccess) return KD_ERR_CUDA;
+  if (N == 0) return KD_OK;
+  const Layout L = plan(N, D, V, K, 0);
+  if (ws_bytes < L.fwd_end) return KD_ERR_WORKSPACE;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int2* pairs = reinterpret_cast<int2*>(w + L.pairs);
+  float* ent = reinterpret_cast<float*>(w + L.ent);
+  float2* part = reinterpret_cast<float2*>(w + L.part);
+  float* zk = reinterpret_cast<float*>(w + L.zk);
+  const float inv_T = 1.0f / T;
+
+  kd_prep_kernel<<<static_cast<unsigned>(cdiv(N, kPrepWarps)), kPrepWarps * 32, 0, s>>>(
+      topk_idx, topk_logit, mask, N, K, V, inv_T, pairs, ent,
+      reinterpret_cast<unsigned long long*>(n_valid), di->status);
+  if ((st = cuda_check()) != KD_OK) return st;
+
+  CUtensorMap mH, mW;
+  if (!make_map(&mH, H, D, N, static_cast<uint64_t>(D) * 2, kBK, kBM) ||
+      !make_map(&mW, W, D, V, static_cast<uint64_t>(D) * 2, kBK, kBNMax))
+    return KD_ERR_CUDA;
+  const int MB = static_cast<int>(cdiv(N, kBM));
+  const int KB = static_cast<int>(cdiv(D, kBK));
+  GemmArgs a = base_args(di);
+  a.sched = make_panel_sched(MB, L.NB, KB, di->num_sms);
+  a.M = static_cast<int>(N);
+  a.Ncols = V;
+  a.BN = kBNMax;
+  a.idesc = umma_idesc_bf16(kBM, kBNMax, false, false);
+  a.K = K;
+  a.scale2 = 1.4426950408889634f * inv_T;
+  a.inv_T = inv_T;
+  a.pairs = pairs;
+  a.zk = zk;
+  a.part = part;
+  a.slots = L.slots;
+  if ((st = launch_gemm<kEpiFwd, false, false>(mH, mW, a, di->num_sms, s)) != KD_OK) return st;
+
+  kd_combine_kernel<<<static_cast<unsigned>(cdiv(N, 256)), 256, 0, s>>>(
+      a.sched, part, L.slots, pairs, zk, ent, mask, N, K, V, inv_T, loss, lse);
+  return cuda_check();
+}
+
+extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                                    const float* topk_logit, const uint8_t* mask, const float* lse,
+                                    const float* dloss, int64_t N, int D, int V, int K, float T,
+                                    int64_t chunk_tokens, int accumulate_dW, uint16_t* dH,
+                                    float* dW, void* ws, size_t ws_bytes, kd_stream_t stream) {
+  kd_status st = check_common(H, W, topk_idx, topk_logit, N, D, V, K, T, ws);
+  if (st != KD_OK) return st;
+  if (!dW || (N > 0 && (!lse || !dloss || !dH))) return KD_ERR_ARG;
+  if (!aligned(dW, 16) || !aligned(dH, 16) || !aligned(lse, 4) || !aligned(dloss, 4))
+    return KD_ERR_ALIGN;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    if (!accumulate_dW &&
+        cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * D * sizeof(float), s) != cudaSuccess)
+      return KD_ERR_CUDA;
+    return KD_OK;
+  }
+  const Layout L = plan(N, D, V, K, chunk_tokens);
+  if (ws_bytes < L.bwd_end) return KD_ERR_WORKSPACE;
+  const int KS = ksplit_that_fits(L, D, ws_bytes, wanted_ksplit(L.C_pad, D, V, di->num_sms));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int2* pairs = reinterpret_cast<int2*>(w + L.pairs);
+  float* ent = reinterpret_cast<float*>(w + L.ent);
+  uint16_t* dz = reinterpret_cast<uint16_t*>(w + L.dz);
+  float* dhp = reinterpret_cast<float*>(w + L.dhp);
+  const float inv_T = 1.0f / T;
+
+  kd_prep_kernel<<<static_cast<unsigned>(cdiv(N, kPrepWarps)), kPrepWarps * 32, 0, s>>>(
+      topk_idx, topk_logit, mask, N, K, V, inv_T, pairs, ent, nullptr, di->status);
+  if ((st = cuda_check()) != KD_OK) return st;
+
+  const int BNd = hidden_tile_width(D);
+  const int NBd = static_cast<int>(cdiv(D, BNd));
+  CUtensorMap mH_k, mW_k, mDz_k, mW_mn, mDz_mn, mH_mn;
+  const uint64_t rowH = static_cast<uint64_t>(D) * 2;
+  const uint64_t rowDz = static_cast<uint64_t>(L.dz_ld) * 2;
+  if (!make_map(&mH_k, H, D, N, rowH, kBK, kBM) || !make_map(&mW_k, W, D, V, rowH, kBK, kBNMax) ||
+      !make_map(&mDz_k, dz, V, L.C_pad, rowDz, kBK, kBM) ||
+      !make_map(&mW_mn, W, D, V, rowH, 64, kBK) || !make_map(&mDz_mn, dz, V, L.C_pad, rowDz, 64, kBK) ||
+      !make_map(&mH_mn, H, D, N, rowH, 64, kBK))
+    return KD_ERR_CUDA;
+
+  const int KBd = static_cast<int>(cdiv(D, kBK));
+  const int KBv = static_cast<int>(cdiv(V, kBK));
+  const int MBv = static_cast<int>(cdiv(V, kBM));
+  for (int64_t c0 = 0; c0 < N; c0 += L.C) {
+    const int64_t rows = (N - c0) < L.C ? (N - c0) : L.C;
+    const int MBc = static_cast<int>(cdiv(rows, kBM));
+
+    // 1. recompute the chunk's logits, dZ epilogue -> dz (bf16)
+    GemmArgs a = base_args(di);
+    a.sched = make_panel_sched(MBc, L.NB, KBd, di->num_sms);
+    a.M = static_cast<int>(rows);
+    a.Ncols = V;
+    a.BN = kBNMax;
+    a.idesc = umma_idesc_bf16(kBM, kBNMax, false, false);
+    a.a_row_off = static_cast<int>(c0);
+    a.row_base = c0;
+    a.K = K;
+    a.scale2 = 1.4426950408889634f * inv_T;
+    a.inv_T = inv_T;
+    a.pairs = pairs;
+    a.lse = lse;
+    a.dloss = dloss;
+    a.mask = mask;
+    a.dz = dz;
+    a.dz_ld = L.dz_ld;
+    if ((st = launch_gemm<kEpiDz, false, false>(mH_k, mW_k, a, di->num_sms, s)) != KD_OK) return st;
+
+    // 2. dH rows of the chunk = dZ W (contraction over V, split KS ways)
+    GemmArgs h = base_args(di);
+    h.sched = make_tile_sched(MBc, NBd, KBv, KS);
+    h.M = static_cast<int>(rows);
+    h.Ncols = D;
+    h.BN = BNd;
+    h.idesc = umma_idesc_bf16(kBM, BNd, false, true);
+    h.row_base = c0;
+    h.out_bf16 = dH;
+    h.out_f32 = dhp;
+    h.part_stride = L.C_pad * static_cast<int64_t>(D);
+    if ((st = launch_gemm<kEpiDh, false, true>(mDz_k, mW_mn, h, di->num_sms, s)) != KD_OK) return st;
+    if (h.sched.KS > 1) {
+      const int64_t groups = rows * (D / 8);
+      int64_t blocks = cdiv(groups, 256);
+      if (blocks > 8L * di->num_sms) blocks = 8L * di->num_sms;
+      kd_dh_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+          dhp, h.sched.KS, h.part_stride, rows, D, dH + c0 * D);
+      if ((st = cuda_check()) != KD_OK) return st;
+    }
+
+    // 3. dW (+)= dZ^T H over the chunk's tokens
+    GemmArgs g = base_args(di);
+    g.sched = make_tile_sched(MBv, NBd, static_cast<int>(cdiv(rows, kBK)), 1);
+    g.M = V;
+    g.Ncols = D;
+    g.BN = BNd;
+    g.idesc = umma_idesc_bf16(kBM, BNd, true, true);
+    g.b_k_off = static_cast<int>(c0);
+    g.out_f32 = dW;
+    g.ld_out = D;
+    g.accumulate = (c0 > 0 || accumulate_dW) ? 1 : 0;
+    if ((st = launch_gemm<kEpiDw, true, true>(mDz_mn, mH_mn, g, di->num_sms, s)) != KD_OK) return st;
+  }
+  return KD_OK;
+}
+
+extern "C" kd_status kd_get_status(kd_stream_t stream) {
+  kd_status st = KD_OK;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return KD_ERR_CUDA;
+  }
+  int v = 0;
+  if (cudaMemcpy(&v, di->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KD_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return KD_ERR_CUDA;
+  return static_cast<kd_status>(v);
+}
+
+extern "C" const char* kd_status_string(kd_status status) {
+  switch (status) {
+    case KD_OK: return "ok";
+    case KD_ERR_ARG: return "invalid argument (size, NULL pointer or temperature)";
+    case KD_ERR_ALIGN: return "pointer alignment violates the ABI rules";
+    case KD_ERR_UNSUPPORTED: return "unsupported shape or device (needs an sm_103 GPU)";
+    case KD_ERR_WORKSPACE: return "workspace smaller than kd_topk_kl_workspace_size()";
+    case KD_ERR_INDEX: return "teacher id outside [0, V) at a counted row";
+    case KD_ERR_TIMEOUT: return "bounded pipeline wait ran out; results are invalid";
+    case KD_ERR_CUDA: return "CUDA runtime or driver call failed";
+  }
+  return "unknown status";
+}
+
+// ------------------------------------------------------------------ test hooks
+
+extern "C" kd_status kd_debug_gemm_bf16(const uint16_t* A, const uint16_t* B, float* C, int M, int N,
+                                        int K, int a_mn, int b_mn, kd_stream_t stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || M % 8 || N % 8 || K % 8) return KD_ERR_ARG;
+  if (!A || !B || !C) return KD_ERR_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return KD_ERR_ALIGN;
+  if (a_mn && !b_mn) return KD_ERR_UNSUPPORTED;
+  kd_status st = KD_OK;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int BN = b_mn ? hidden_tile_width(N) : kBNMax;
+  CUtensorMap ma, mb;
+  bool ok;
+  if (!a_mn)
+    ok = make_map(&ma, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM);
+  else
+    ok = make_map(&ma, A, M, K, static_cast<uint64_t>(M) * 2, 64, kBK);
+  if (!b_mn)
+    ok = ok && make_map(&mb, B, K, N, static_cast<uint64_t>(K) * 2, kBK, kBNMax);
+  else
+    ok = ok && make_map(&mb, B, N, K, static_cast<uint64_t>(N) * 2, 64, kBK);
+  if (!ok) return KD_ERR_CUDA;
+  GemmArgs a = base_args(di);
+  a.sched = make_tile_sched(static_cast<int>(cdiv(M, kBM)), static_cast<int>(cdiv(N, BN)),
+                            static_cast<int>(cdiv(K, kBK)), 1);
+  a.M = M;
+  a.Ncols = N;
+  a.BN = BN;
+  a.idesc = umma_idesc_bf16(kBM, BN, a_mn != 0, b_mn != 0);
+  a.out_f32 = C;
+  a.ld_out = N;
+  if (!a_mn && !b_mn) return launch_gemm<kEpiPlain, false, false>(ma, mb, a, di->num_sms, s);
+  if (!a_mn && b_mn) return launch_gemm<kEpiPlain, false, true>(ma, mb, a, di->num_sms, s);
+  return launch_gemm<kEpiPlain, true, true>(ma, mb, a, di->num_sms, s);
+}
+
+extern "C" kd_status kd_debug_wait_timeout(uint64_t timeout_ns, kd_stream_t stream) {
+  kd_status st = KD_OK;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  if (timeout_ns > 2000000000ull) timeout_ns = 2000000000ull;
+  kd_wait_probe_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(timeout_ns, di->status);
+  return cuda_check();
+}
+
+extern "C" kd_status kd_debug_schedule(int kind, int64_t rows, int64_t cols, int64_t depth,
+                                       int num_sms, int32_t* counts, int64_t* info) {
+  if (rows <= 0 || cols <= 0 || depth <= 0 || num_sms <= 0 || kind < 0 || kind > 2 || !info)
+    return KD_ERR_ARG;
+  const int MB = static_cast<int>(cdiv(rows, kBM));
+  const int KB = static_cast<int>(cdiv(depth, kBK));
+  int BN, NB;
+  Sched sc;
+  if (kind == 0) {
+    BN = kBNMax;
+    NB = static_cast<int>(cdiv(cols, BN));
+    sc = make_panel_sched(MB, NB, KB, num_sms);
+  } else {
+    BN = hidden_tile_width(static_cast<int>(cols));
+    NB = static_cast<int>(cdiv(cols, BN));
+    const int ks = (kind == 1) ? choose_ksplit(static_cast<int64_t>(MB) * NB, KB, num_sms) : 1;
+    sc = make_tile_sched(MB, NB, KB, ks);
+  }
+  const int64_t grid = sc.total < num_sms ? sc.total : num_sms;
+  int max_slot = 0;
+  for (int64_t u = 0; u < sc.total; ++u) {
+    const Unit d = sched_unit(sc, u);
+    if (d.slot + 1 > max_slot) max_slot = d.slot + 1;
+    if (counts)
+      for (int nb = d.n_begin; nb < d.n_end; ++nb)
+        for (int kb = d.kb_begin; kb < d.kb_end; ++kb)
+          counts[(static_cast<int64_t>(d.m_blk) * NB + nb) * KB + kb] += 1;
+  }
+  info[0] = sc.total;
+  info[1] = grid;
+  info[2] = MB;
+  info[3] = NB;
+  info[4] = KB;
+  info[5] = BN;
+  info[6] = max_slot;
+  info[7] = sc.KS;
+  return KD_OK;
+}
