@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""Benchmark of the fused top-K KL distillation head (forward + backward).
+
+One step = one forward (kd_topk_kl_fwd) and one backward (kd_topk_kl_bwd) over
+one batch of synthetic inputs of the named workload, all in the CUDA library.
+Default workload: the long-context gpt-oss-shaped head, N = 32,768 tokens
+(batch 1 x seq 32,768), D = 2,880, V = 201,088, K = 64, T = 1, 2% of rows masked.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU fp64 oracle, timed on host cores
+  python bench.py --sweep                # peak memory and rate for N = 4K ... 256K
+
+Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an
+independent replica on its own GPU (the head needs no exchange between
+replicas); the barrier-bracketed time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused top-K KL head fwd+bwd tokens/s & TFLOP/s (% bf16 peak); peak GB vs N"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+GEMM_CATS = ("fwd_gemm", "dz_gemm", "dh_gemm", "dw_gemm")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gptoss_32k")
+    ap.add_argument("--chunk", type=int, default=4096)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(p, chunk):
+    return {
+        "workload": f"{p.name}: N={p.N} tokens, D={p.D}, V={p.V}, K={p.K}, T={p.T}",
+        "N": p.N, "D": p.D, "V": p.V, "K": p.K, "T": p.T,
+        "masked_rows": int(p.N - int(p.mask.sum().item())),
+        "chunk_tokens": chunk,
+        "l2": "inputs larger than L2 (W alone is %.2f GB; every pass streams it)" % (p.V * p.D * 2 / 1e9),
+        "inputs": "H ~ N(0,1), W ~ N(0,1/D) in bf16; teacher ids distinct uniform, logits N(0,4)+Gumbel sorted",
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader",
+                                          "-lms", "200"] + sel, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def mhz(x):
+            try:
+                return float(x.split()[0])
+            except Exception:
+                return None
+
+        sm = [mhz(r[1]) for r in rows if mhz(r[1])]
+        mx = [mhz(r[2]) for r in rows if mhz(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        busy = [s for s in sm if mx and s > 0.3 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------------- CPU oracle
+
+def oracle_rate(p, seconds: float, seed: int = 0, max_rows: int = 1024):
+    """Oracle fwd+bwd on a seeded sample of rows; returns (tokens/s, rows, secs, threads)."""
+    import numpy as np
+
+    import oracle
+
+    W64 = p.W.double().cpu().numpy()           # input conversion, outside the timed part
+    H = p.H.cpu()
+    m = p.mask.cpu().numpy()
+    idx = p.idx.cpu().numpy()
+    t = p.t.double().cpu().numpy()
+    nv = max(int(m.sum()), 1)
+    rng = np.random.default_rng(seed)
+
+    def run(n):
+        rows = np.sort(rng.choice(p.N, size=min(n, p.N), replace=False))
+        Hs = H[rows].double().numpy()
+        g = m[rows].astype(np.float64) / nv
+        t0 = time.perf_counter()
+        oracle.kd_forward(Hs, W64, idx[rows], t[rows], m[rows], p.T)
+        oracle.kd_backward(Hs, W64, idx[rows], t[rows], m[rows], p.T, g)
+        return len(rows), time.perf_counter() - t0
+
+    n0, s0 = run(8)
+    n = int(min(max_rows, max(8, 8 * seconds / max(s0, 1e-3))))
+    n1, s1 = run(n)
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max(int(d.get("num_threads", 1)) for d in threadpool_info()) or os.cpu_count()
+    except Exception:
+        threads = os.cpu_count()
+    return n1 / s1, n1, s1, threads
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import torch
+
+    from workloads import config_problem
+    p = config_problem(args.workload, seed=args.seed, device="cpu")
+    import numpy as np
+
+    import oracle
+    W64 = p.W.double().numpy()
+    m = p.mask.numpy()
+    idx = p.idx.numpy()
+    t = p.t.double().numpy()
+    nv = max(int(m.sum()), 1)
+    rows_per_step = 16
+    rng = np.random.default_rng(args.seed)
+    times = []
+    for i in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(p.N, size=rows_per_step, replace=False))
+        Hs = p.H[rows].double().numpy()
+        t0 = time.perf_counter()
+        oracle.kd_forward(Hs, W64, idx[rows], t[rows], m[rows], p.T)
+        oracle.kd_backward(Hs, W64, idx[rows], t[rows], m[rows], p.T, m[rows] / nv)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    rate = rows_per_step * args.steps / total
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max(int(d.get("num_threads", 1)) for d in threadpool_info())
+    except Exception:
+        threads = os.cpu_count()
+    sample = (f"{rows_per_step} seeded rows of {p.N} per step (fwd+bwd over the full V={p.V}); "
+              f"the oracle is row-additive so rows/s is its tokens/s")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_desc(p, args.chunk),
+        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": f"CPU fp64 oracle (numpy/OpenBLAS) on host cores; one step = {rows_per_step} rows",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------- CUDA path
+
+class Head:
+    """Device buffers and the fwd+bwd step of one replica."""
+
+    def __init__(self, p, chunk):
+        import torch
+
+        from top_kl_loss_lm_b300 import binding
+        self.b = binding
+        self.p = p
+        self.chunk = chunk
+        dev = p.H.device
+        N, D, V, K = p.N, p.D, p.V, p.K
+        self.ws = torch.empty(binding.kd_topk_kl_workspace_size(N, D, V, K, chunk), dtype=torch.uint8,
+                              device=dev)
+        self.loss = torch.empty(N, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(N, dtype=torch.float32, device=dev)
+        self.nv = torch.empty(1, dtype=torch.int64, device=dev)
+        self.dH = torch.empty_like(p.H)
+        self.dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+        from workloads import mean_upstream_grad
+        self.g = mean_upstream_grad(p.mask).to(dev)
+
+    def step(self, H=None, idx=None, t=None, mask=None, g=None):
+        p = self.p
+        H = p.H if H is None else H
+        idx = p.idx if idx is None else idx
+        t = p.t if t is None else t
+        mask = p.mask if mask is None else mask
+        g = self.g if g is None else g
+        self.b.kd_topk_kl_fwd(H, p.W, idx, t, mask, p.T, self.loss, self.lse, self.nv, self.ws)
+        self.b.kd_topk_kl_bwd(H, p.W, idx, t, mask, self.lse, g, p.T, self.chunk, False, self.dH,
+                              self.dW, self.ws)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    from top_kl_loss_lm_b300 import binding
+    from workloads import config_problem
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    p = config_problem(args.workload, seed=args.seed + rank, device=dev)
+    head = Head(p, args.chunk)
+    N, D, V = p.N, p.D, p.V
+    flops_step = 8.0 * N * D * V
+
+    for _ in range(max(args.warmup, 3)):
+        head.step()
+    st = binding.kd_get_status()
+    if st != 0:
+        raise RuntimeError(f"device status {binding.STATUS.get(st, st)} after warm-up")
+
+    # ------------------------------------------------ device-timed region
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    sampler.start()
+    binding.kd_debug_profile(True)
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        head.step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    prof = binding.kd_debug_profile_read()
+    binding.kd_debug_profile(False)
+    ms = e0.elapsed_time(e1)
+    st = binding.kd_get_status()
+    if st != 0:
+        raise RuntimeError(f"device status {binding.STATUS.get(st, st)} in the timed region")
+    peak_mem = torch.cuda.max_memory_allocated()
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * N * args.steps / (ms / 1000.0)
+    tflops = world * flops_step * args.steps / (ms / 1000.0) / 1e12
+
+    # ------------------------------------------------ end to end from host buffers
+    e2e = None
+    if not args.no_e2e:
+        hH = p.H.cpu().pin_memory()
+        hidx = p.idx.cpu().pin_memory()
+        ht = p.t.cpu().pin_memory()
+        hm = p.mask.cpu().pin_memory()
+        hg = head.g.cpu().pin_memory()
+        hloss = torch.empty(N, dtype=torch.float32).pin_memory()
+        hnv = torch.empty(1, dtype=torch.int64).pin_memory()
+        dH_in = torch.empty_like(p.H)
+        didx = torch.empty_like(p.idx)
+        dt = torch.empty_like(p.t)
+        dm = torch.empty_like(p.mask)
+        dg = torch.empty_like(head.g)
+
+        def e2e_step():
+            dH_in.copy_(hH, non_blocking=True)
+            didx.copy_(hidx, non_blocking=True)
+            dt.copy_(ht, non_blocking=True)
+            dm.copy_(hm, non_blocking=True)
+            dg.copy_(hg, non_blocking=True)
+            head.step(H=dH_in, idx=didx, t=dt, mask=dm, g=dg)
+            hloss.copy_(head.loss, non_blocking=True)
+            hnv.copy_(head.nv, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([ems], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ems = float(tt.item())
+        h2d = sum(x.numel() * x.element_size() for x in (hH, hidx, ht, hm, hg))
+        d2h = hloss.numel() * 4 + 8
+        e2e = {"value": world * N * args.steps / (ems / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "note": "H, teacher ids/logits, mask and upstream grad copied from pinned host memory "
+                       "each step; per-row loss and n_valid read back; W, dH, dW stay resident"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    # ------------------------------------------------ roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    kernels = {}
+    for c, (tot, n) in prof.items():
+        if n == 0:
+            continue
+        entry = {"ms_per_step": tot / args.steps, "launches_per_step": n / args.steps,
+                 "share": None}
+        if c in GEMM_CATS:
+            entry["tflops"] = 2.0 * N * D * V * args.steps / (tot / 1000.0) / 1e12
+        kernels[c] = entry
+    total_k = sum(prof[c][0] for c in prof)
+    for c in kernels:
+        kernels[c]["share"] = prof[c][0] / total_k if total_k else None
+    dom = max((c for c in kernels if c in GEMM_CATS), key=lambda c: prof[c][0])
+    tot, n = prof[dom]
+    flops_per_launch = 2.0 * N * D * V * args.steps / n
+    achieved = flops_per_launch / (tot / n / 1000.0) / 1e12
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sus,
+                "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": None,
+                "peak_kind": f"sustained bf16 dense ({peak_src}); kernel timed inside a long step",
+                "frac_of_burst": achieved / peak_burst,
+                "flops_per_launch": flops_per_launch}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, nrows, secs, threads = oracle_rate(p, args.cpu_seconds, seed=args.seed)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{nrows} seeded rows of {N} (fwd+bwd over the full V={V}), {secs:.1f} s; "
+                         f"W converted to fp64 outside the timed part"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_desc(p, args.chunk), parallelism=f"replicas x{world}"),
+        "tflops": tflops, "frac_of_bf16_peak": {"burst": tflops / world / peak_burst,
+                                                "sustained": tflops / world / peak_sus},
+        "peak_mem_gb": peak_mem / 1e9,
+        "roofline": roofline, "kernels": kernels,
+        "gpu_launches": int(sum(n for _, n in prof.values())),
+        "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_sweep(args):
+    """Peak device memory and rate vs N (D, V, K of the gpt-oss head)."""
+    import torch
+
+    from workloads import make_problem
+    for N in (4096, 16384, 65536, 131072, 262144):
+        p = make_problem(N, 2880, 201088, 64, 1.0, seed=args.seed, mask="frac", mask_frac=0.02,
+                         device="cuda", name=f"sweep_{N}")
+        torch.cuda.synchronize()
+        torch.cuda.reset_peak_memory_stats()
+        head = Head(p, args.chunk)
+        for _ in range(2):
+            head.step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        steps = 3
+        e0.record()
+        for _ in range(steps):
+            head.step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        print(json.dumps({"sweep": True, "N": N, "ms_per_step": ms, "tokens_per_s": N / (ms / 1e3),
+                          "tflops": 8.0 * N * 2880 * 201088 / (ms / 1e3) / 1e12,
+                          "peak_mem_gb": torch.cuda.max_memory_allocated() / 1e9,
+                          "workspace_gb": head.ws.numel() / 1e9,
+                          "dense_grid_bf16_gb": N * 201088 * 2 / 1e9}), flush=True)
+        del head, p
+        torch.cuda.empty_cache()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if args.sweep:
+        return run_sweep(args)
+    return run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -49,6 +49,18 @@ kd_status kd_debug_wait_timeout(uint64_t timeout_ns, kd_stream_t stream);
 kd_status kd_debug_schedule(int kind, int64_t rows, int64_t cols, int64_t depth, int num_sms,
                             int32_t* counts, int64_t* info);
 
+/*
+ * Per-kernel timing. enable != 0 starts recording a CUDA event pair on the
+ * launching stream around every kernel the library launches (clearing earlier
+ * records); enable = 0 stops. kd_debug_profile_read waits for the recorded
+ * events and returns, per category, the summed milliseconds and the launch
+ * count (arrays of length n; categories: 0 prep, 1 forward GEMM, 2 combine,
+ * 3 dZ GEMM, 4 dH GEMM, 5 dH split sum, 6 dW GEMM), then clears the records.
+ * Event objects are created on first use and kept for the process lifetime.
+ */
+kd_status kd_debug_profile(int enable);
+kd_status kd_debug_profile_read(double* total_ms, int64_t* launches, int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,6 +20,7 @@ __all__ = [
     "kd_topk_kl_workspace_size", "kd_topk_kl_fwd", "kd_topk_kl_bwd",
     "kd_get_status", "kd_status_string",
     "kd_debug_gemm_bf16", "kd_debug_wait_timeout", "kd_debug_schedule",
+    "kd_debug_profile", "kd_debug_profile_read", "PROFILE_CATEGORIES",
     "STATUS",
 ]
 
@@ -72,6 +73,10 @@ def lib() -> ctypes.CDLL:
         L.kd_debug_wait_timeout.restype = i32
         L.kd_debug_schedule.argtypes = [i32, i64, i64, i64, i32, vp, vp]
         L.kd_debug_schedule.restype = i32
+        L.kd_debug_profile.argtypes = [i32]
+        L.kd_debug_profile.restype = i32
+        L.kd_debug_profile_read.argtypes = [vp, vp, i32]
+        L.kd_debug_profile_read.restype = i32
         _LIB = L
         return L
 
@@ -190,3 +195,20 @@ def kd_debug_schedule(kind: int, rows: int, cols: int, depth: int, num_sms: int,
         counts = counts.reshape(MB, NB, KB)
     keys = ["units", "grid", "MB", "NB", "KB", "BN", "max_slots", "k_splits"]
     return {k: int(v) for k, v in zip(keys, info)}, counts
+
+
+PROFILE_CATEGORIES = ["prep", "fwd_gemm", "combine", "dz_gemm", "dh_gemm", "dh_sum", "dw_gemm"]
+
+
+def kd_debug_profile(enable: bool):
+    _check(lib().kd_debug_profile(1 if enable else 0), "kd_debug_profile")
+
+
+def kd_debug_profile_read():
+    """{category: (total_ms, launches)} for the records since kd_debug_profile(True)."""
+    import numpy as np
+    n = len(PROFILE_CATEGORIES)
+    ms = np.zeros(n, dtype=np.float64)
+    cnt = np.zeros(n, dtype=np.int64)
+    _check(lib().kd_debug_profile_read(ms.ctypes.data, cnt.ctypes.data, n), "kd_debug_profile_read")
+    return {c: (float(ms[i]), int(cnt[i])) for i, c in enumerate(PROFILE_CATEGORIES)}

@@ -15,6 +15,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/kd_topk_kl.h"
 #include "../../include/kd_topk_kl_testing.h"
@@ -40,6 +41,43 @@ struct DevInfo {
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Optional per-launch timing (test hook kd_debug_profile): a start/stop event
+// pair recorded on the launching stream around every kernel of the library.
+enum ProfCat : int { kProfPrep = 0, kProfFwdGemm, kProfCombine, kProfDzGemm, kProfDhGemm, kProfDhSum,
+                     kProfDwGemm, kProfCats };
+struct Prof {
+  bool on = false;
+  std::vector<cudaEvent_t> ev;      // pool: 2 per record
+  std::vector<int> cat;             // category of record i
+  size_t used = 0;
+};
+Prof g_prof;
+
+struct ProfScope {
+  cudaStream_t s;
+  int rec = -1;
+  ProfScope(int c, cudaStream_t st) : s(st) {
+    if (!g_prof.on) return;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_prof.used * 2 + 2 > g_prof.ev.size()) {
+      cudaEvent_t a, b;
+      if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+      }
+      g_prof.ev.push_back(a);
+      g_prof.ev.push_back(b);
+    }
+    rec = static_cast<int>(g_prof.used++);
+    if (g_prof.cat.size() < g_prof.used) g_prof.cat.resize(g_prof.used);
+    g_prof.cat[rec] = c;
+    cudaEventRecord(g_prof.ev[2 * rec], s);
+  }
+  ~ProfScope() {
+    if (rec >= 0) cudaEventRecord(g_prof.ev[2 * rec + 1], s);
+  }
+};
 
 const DevInfo* device_info(kd_status* err) {
   int dev = 0;
@@ -248,9 +286,12 @@ extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const 
   float* zk = reinterpret_cast<float*>(w + L.zk);
   const float inv_T = 1.0f / T;
 
-  kd_prep_kernel<<<static_cast<unsigned>(cdiv(N, kPrepWarps)), kPrepWarps * 32, 0, s>>>(
-      topk_idx, topk_logit, mask, N, K, V, inv_T, pairs, ent,
-      reinterpret_cast<unsigned long long*>(n_valid), di->status);
+  {
+    ProfScope ps(kProfPrep, s);
+    kd_prep_kernel<<<static_cast<unsigned>(cdiv(N, kPrepWarps)), kPrepWarps * 32, 0, s>>>(
+        topk_idx, topk_logit, mask, N, K, V, inv_T, pairs, ent,
+        reinterpret_cast<unsigned long long*>(n_valid), di->status);
+  }
   if ((st = cuda_check()) != KD_OK) return st;
 
   CUtensorMap mH, mW;
@@ -272,10 +313,15 @@ extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const 
   a.zk = zk;
   a.part = part;
   a.slots = L.slots;
-  if ((st = launch_gemm<kEpiFwd, false, false>(mH, mW, a, di->num_sms, s)) != KD_OK) return st;
-
-  kd_combine_kernel<<<static_cast<unsigned>(cdiv(N, 256)), 256, 0, s>>>(
-      a.sched, part, L.slots, pairs, zk, ent, mask, N, K, V, inv_T, loss, lse);
+  {
+    ProfScope ps(kProfFwdGemm, s);
+    if ((st = launch_gemm<kEpiFwd, false, false>(mH, mW, a, di->num_sms, s)) != KD_OK) return st;
+  }
+  {
+    ProfScope ps(kProfCombine, s);
+    kd_combine_kernel<<<static_cast<unsigned>(cdiv(N, 256)), 256, 0, s>>>(
+        a.sched, part, L.slots, pairs, zk, ent, mask, N, K, V, inv_T, loss, lse);
+  }
   return cuda_check();
 }
 
@@ -308,8 +354,11 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
   float* dhp = reinterpret_cast<float*>(w + L.dhp);
   const float inv_T = 1.0f / T;
 
-  kd_prep_kernel<<<static_cast<unsigned>(cdiv(N, kPrepWarps)), kPrepWarps * 32, 0, s>>>(
-      topk_idx, topk_logit, mask, N, K, V, inv_T, pairs, ent, nullptr, di->status);
+  {
+    ProfScope ps(kProfPrep, s);
+    kd_prep_kernel<<<static_cast<unsigned>(cdiv(N, kPrepWarps)), kPrepWarps * 32, 0, s>>>(
+        topk_idx, topk_logit, mask, N, K, V, inv_T, pairs, ent, nullptr, di->status);
+  }
   if ((st = cuda_check()) != KD_OK) return st;
 
   const int BNd = hidden_tile_width(D);
@@ -348,7 +397,10 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     a.mask = mask;
     a.dz = dz;
     a.dz_ld = L.dz_ld;
-    if ((st = launch_gemm<kEpiDz, false, false>(mH_k, mW_k, a, di->num_sms, s)) != KD_OK) return st;
+    {
+      ProfScope ps(kProfDzGemm, s);
+      if ((st = launch_gemm<kEpiDz, false, false>(mH_k, mW_k, a, di->num_sms, s)) != KD_OK) return st;
+    }
 
     // 2. dH rows of the chunk = dZ W (contraction over V, split KS ways)
     GemmArgs h = base_args(di);
@@ -361,11 +413,15 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     h.out_bf16 = dH;
     h.out_f32 = dhp;
     h.part_stride = L.C_pad * static_cast<int64_t>(D);
-    if ((st = launch_gemm<kEpiDh, false, true>(mDz_k, mW_mn, h, di->num_sms, s)) != KD_OK) return st;
+    {
+      ProfScope ps(kProfDhGemm, s);
+      if ((st = launch_gemm<kEpiDh, false, true>(mDz_k, mW_mn, h, di->num_sms, s)) != KD_OK) return st;
+    }
     if (h.sched.KS > 1) {
       const int64_t groups = rows * (D / 8);
       int64_t blocks = cdiv(groups, 256);
       if (blocks > 8L * di->num_sms) blocks = 8L * di->num_sms;
+      ProfScope ps(kProfDhSum, s);
       kd_dh_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
           dhp, h.sched.KS, h.part_stride, rows, D, dH + c0 * D);
       if ((st = cuda_check()) != KD_OK) return st;
@@ -382,7 +438,10 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     g.out_f32 = dW;
     g.ld_out = D;
     g.accumulate = (c0 > 0 || accumulate_dW) ? 1 : 0;
-    if ((st = launch_gemm<kEpiDw, true, true>(mDz_mn, mH_mn, g, di->num_sms, s)) != KD_OK) return st;
+    {
+      ProfScope ps(kProfDwGemm, s);
+      if ((st = launch_gemm<kEpiDw, true, true>(mDz_mn, mH_mn, g, di->num_sms, s)) != KD_OK) return st;
+    }
   }
   return KD_OK;
 }
@@ -499,5 +558,39 @@ extern "C" kd_status kd_debug_schedule(int kind, int64_t rows, int64_t cols, int
   info[5] = BN;
   info[6] = max_slot;
   info[7] = sc.KS;
+  return KD_OK;
+}
+
+extern "C" kd_status kd_debug_profile(int enable) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof.on = enable != 0;
+  g_prof.used = 0;
+  return KD_OK;
+}
+
+extern "C" kd_status kd_debug_profile_read(double* total_ms, int64_t* launches, int n) {
+  if (!total_ms || !launches || n < 1) return KD_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < n; ++i) {
+    total_ms[i] = 0.0;
+    launches[i] = 0;
+  }
+  for (size_t r = 0; r < g_prof.used; ++r) {
+    if (cudaEventSynchronize(g_prof.ev[2 * r + 1]) != cudaSuccess) {
+      cudaGetLastError();
+      return KD_ERR_CUDA;
+    }
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, g_prof.ev[2 * r], g_prof.ev[2 * r + 1]) != cudaSuccess) {
+      cudaGetLastError();
+      return KD_ERR_CUDA;
+    }
+    const int c = g_prof.cat[r];
+    if (c < n) {
+      total_ms[c] += ms;
+      launches[c] += 1;
+    }
+  }
+  g_prof.used = 0;
   return KD_OK;
 }

@@ -68,8 +68,8 @@ def _distinct_indices(N: int, V: int, K: int, g: torch.Generator, device) -> tor
     """K distinct ids per row, uniform over [0, V), in random (cache) order."""
     if K > V:
         raise ValueError("K must not exceed V")
-    if 4 * K > V:
-        # dense case: a random permutation prefix per row
+    if K * K > V:
+        # many collisions expected: a random permutation prefix per row
         keys = torch.rand(N, V, generator=g, device=device)
         return keys.argsort(dim=1)[:, :K].to(torch.int32).contiguous()
     idx = torch.randint(0, V, (N, K), generator=g, device=device, dtype=torch.int64)
@@ -160,6 +160,9 @@ CONFIGS = {
                       mask_frac=0.02),
     "gptoss_32k": dict(N=32768, D=2880, V=201088, K=64, T=1.0, teacher="gumbel", mask="frac",
                        mask_frac=0.02),
+    # small profiling case: same D and K as the gpt-oss head, W still larger than L2
+    "profile_small": dict(N=4096, D=2880, V=32768, K=64, T=1.0, teacher="gumbel", mask="frac",
+                          mask_frac=0.02),
     "packed_qwen": dict(N=32768, D=4096, V=151936, K=64, T=1.0, teacher="gumbel", mask="packed",
                         garbage_masked=True),
 }
