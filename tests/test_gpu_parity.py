@@ -126,7 +126,7 @@ def test_autograd_wrapper():
     W = p.W.clone().requires_grad_(True)
     loss, nv = fused_topk_kl(H, W, p.idx, p.t, p.mask, p.T)
     (loss.sum() / nv.float()).backward()
-    g = mean_upstream_grad(p.mask).double().numpy()
+    g = mean_upstream_grad(p.mask).double().cpu().numpy()
     ref = P.run_oracle(p, g)
     P.assert_rows_close(loss.detach().cpu().numpy(), ref["loss"], "loss")
     P.assert_grad_close(H.grad.double().cpu().numpy(), ref["dH"], "dH")
