@@ -103,6 +103,33 @@ kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const int32_t* to
                          void* ws, size_t ws_bytes, kd_stream_t stream);
 
 /*
+ * Forward with no workspace argument and no allocation, for callers that
+ * cannot obtain device memory themselves (a plugin inside a process whose own
+ * allocator already holds the GPU's memory, or a hot path where cudaMalloc,
+ * which can synchronise the device, is not allowed). The paper has no
+ * counterpart; this is a convenience of this library.
+ *   - Same arguments and results as kd_topk_kl_fwd, minus ws / ws_bytes. The
+ *     caller still owns and passes every input and output.
+ *   - Scratch comes from a fixed 64 MiB array inside the library's device
+ *     image, held by every GPU that loads the library until the process exits.
+ *     The forward needs N * (12 K + 4 + 8 min(ceil(V / 256), 64)) bytes of it
+ *     (plus 256-byte alignment per region), i.e. at most about 52K tokens at
+ *     K = 64, V = 201,088. Larger sizes are rejected with KD_ERR_WORKSPACE
+ *     before anything is launched.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents (nothing in it has to start at zero: every cell a call reads is
+ *     written earlier in that call). Calls that can overlap on the GPU, e.g. on
+ *     two streams without ordering between them, race on it.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+kd_status kd_topk_kl_fwd_noalloc(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                                 const float* topk_logit, const uint8_t* mask, int64_t N, int D,
+                                 int V, int K, float T, float* loss, float* lse, int64_t* n_valid,
+                                 kd_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word (KD_OK, KD_ERR_INDEX or KD_ERR_TIMEOUT), or KD_ERR_CUDA if the
  * synchronisation itself failed.

@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "KdError", "lib", "library_path",
-    "kd_topk_kl_workspace_size", "kd_topk_kl_fwd", "kd_topk_kl_bwd",
+    "kd_topk_kl_workspace_size", "kd_topk_kl_fwd", "kd_topk_kl_bwd", "kd_topk_kl_fwd_noalloc",
     "kd_get_status", "kd_status_string",
     "kd_debug_gemm_bf16", "kd_debug_wait_timeout", "kd_debug_schedule",
     "kd_debug_profile", "kd_debug_profile_read", "PROFILE_CATEGORIES",
@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.kd_topk_kl_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, i64, i32,
                                      vp, vp, vp, sz, vp]
         L.kd_topk_kl_bwd.restype = i32
+        L.kd_topk_kl_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp, vp]
+        L.kd_topk_kl_fwd_noalloc.restype = i32
         L.kd_get_status.argtypes = [vp]
         L.kd_get_status.restype = i32
         L.kd_status_string.argtypes = [i32]
@@ -133,6 +135,29 @@ def kd_topk_kl_fwd(H, W, topk_idx, topk_logit, mask, T: float, loss, lse, n_vali
         _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream),
     )
     _check(lib().kd_topk_kl_fwd(*args), "kd_topk_kl_fwd")
+
+
+def kd_topk_kl_fwd_noalloc(H, W, topk_idx, topk_logit, mask, T: float, loss, lse, n_valid,
+                           stream=None):
+    """Forward that needs no workspace: the library uses its own fixed device scratch.
+
+    For callers that cannot allocate device memory (see kd_topk_kl_fwd_noalloc in
+    the header for the size limit and the sharing rules).
+    """
+    N, D = H.shape
+    V = W.shape[0]
+    K = topk_idx.shape[1]
+    dev = H.device
+    args = (
+        _ptr(H, torch.bfloat16, (N, D), "H", dev), _ptr(W, torch.bfloat16, (V, D), "W", dev),
+        _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
+        _ptr(topk_logit, torch.float32, (N, K), "topk_logit", dev),
+        _ptr(mask, torch.uint8, (N,), "mask", dev),
+        N, D, V, K, float(T),
+        _ptr(loss, torch.float32, (N,), "loss", dev), _ptr(lse, torch.float32, (N,), "lse", dev),
+        _ptr(n_valid, torch.int64, (1,), "n_valid", dev), _stream(stream),
+    )
+    _check(lib().kd_topk_kl_fwd_noalloc(*args), "kd_topk_kl_fwd_noalloc")
 
 
 def kd_topk_kl_bwd(H, W, topk_idx, topk_logit, mask, lse, dloss, T: float, chunk_tokens: int,

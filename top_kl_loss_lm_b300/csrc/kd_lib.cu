@@ -594,3 +594,54 @@ extern "C" kd_status kd_debug_profile_read(double* total_ms, int64_t* launches, 
   g_prof.used = 0;
   return KD_OK;
 }
+
+// ------------------------------------------------------------------ forward without allocation
+//
+// For callers that cannot allocate device memory themselves: a plugin that
+// runs inside a host process whose allocator has already reserved the GPU's
+// memory, or a latency-critical path where cudaMalloc (which may synchronise
+// the device) is not allowed. The forward's scratch lives in this fixed array
+// instead of a caller workspace. The array is part of the library's device
+// image, so every GPU that loads the library holds its 64 MiB until the
+// process exits.
+namespace {
+constexpr size_t kFwdScratchBytes = size_t(64) << 20;
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_kd_fwd_scratch[kFwdScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kd::kMaxDevices] = {};
+}  // namespace
+
+extern "C" kd_status kd_topk_kl_fwd_noalloc(const uint16_t* H, const uint16_t* W,
+                                            const int32_t* topk_idx, const float* topk_logit,
+                                            const uint8_t* mask, int64_t N, int D, int V, int K,
+                                            float T, float* loss, float* lse, int64_t* n_valid,
+                                            kd_stream_t stream) {
+  if (N < 0 || D <= 0 || V <= 0 || K < 1 || K > kMaxTopK || D % 8 != 0) return KD_ERR_ARG;
+  if (plan(N, D, V, K, 0).fwd_end > kFwdScratchBytes) return KD_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kd::kMaxDevices) {
+    cudaGetLastError();
+    return KD_ERR_CUDA;
+  }
+  void* ws = nullptr;
+  {
+    // Set-up once per device, with that device current: the host-side name of
+    // the array is not a device address, so ask the runtime for the real one.
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_kd_fwd_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return KD_ERR_CUDA;
+      }
+      g_scratch_ptr[dev] = p;
+    }
+    ws = g_scratch_ptr[dev];
+  }
+  return kd_topk_kl_fwd(H, W, topk_idx, topk_logit, mask, N, D, V, K, T, loss, lse, n_valid, ws,
+                        kFwdScratchBytes, stream);
+}
