@@ -22,9 +22,11 @@ extern "C" {
  * row-major (M contiguous). b_mn likewise for B ([N x K] or [K x N]).
  * C is [M x N] fp32 row-major. Device pointers, 16-byte aligned; M, N and K
  * must be multiples of 8. (a_mn, b_mn) = (1, 0) is not supported.
+ * cta_pair != 0 runs the CTA-pair form the loss uses (cta_group::2, 256-row
+ * tiles); 0 runs the single-CTA form (128-row tiles).
  */
 kd_status kd_debug_gemm_bf16(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K,
-                             int a_mn, int b_mn, kd_stream_t stream);
+                             int a_mn, int b_mn, int cta_pair, kd_stream_t stream);
 
 /*
  * Launches one block whose pipeline wait can never be satisfied (nothing
@@ -39,15 +41,16 @@ kd_status kd_debug_wait_timeout(uint64_t timeout_ns, kd_stream_t stream);
  * kind: 0 = forward / dZ recompute (rows x vocabulary tiles),
  *       1 = dH (tokens x hidden tiles, split over the vocabulary),
  *       2 = dW (vocabulary x hidden tiles).
- * rows, cols, depth: the GEMM's M, N (columns) and K extents; num_sms: the
- * SM count to plan for. counts (optional, length MB*NB*KBLOCKS, where MB =
- * ceil(rows/128), NB = number of column tiles, KBLOCKS = ceil(depth/64)) is
- * incremented once per (m-tile, n-tile, k-block) the schedule visits.
- * info (length 8) receives {units, grid, MB, NB, KBLOCKS, BN, max_slots,
- * k_splits}. Returns KD_ERR_ARG for bad sizes.
+ * rows, cols, depth: the GEMM's M, N (columns) and K extents; grid_units:
+ * the number of persistent workers to plan for (SMs, or CTA pairs);
+ * tile_rows: 128 (single CTA) or 256 (CTA pair). counts (optional, length
+ * MB*NB*KBLOCKS, where MB = ceil(rows/tile_rows), NB = number of column
+ * tiles, KBLOCKS = ceil(depth/64)) is incremented once per (m-tile, n-tile,
+ * k-block) the schedule visits. info (length 8) receives {units, grid, MB,
+ * NB, KBLOCKS, BN, max_slots, k_splits}. Returns KD_ERR_ARG for bad sizes.
  */
-kd_status kd_debug_schedule(int kind, int64_t rows, int64_t cols, int64_t depth, int num_sms,
-                            int32_t* counts, int64_t* info);
+kd_status kd_debug_schedule(int kind, int64_t rows, int64_t cols, int64_t depth, int grid_units,
+                            int tile_rows, int32_t* counts, int64_t* info);
 
 /*
  * Per-kernel timing. enable != 0 starts recording a CUDA event pair on the

@@ -104,9 +104,9 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("kind,rows,cols,depth", SHAPES)
-@pytest.mark.parametrize("sms", [148, 132, 7])
-def test_schedule_visits_each_tile_once(lib, kind, rows, cols, depth, sms):
-    info, counts = binding.kd_debug_schedule(kind, rows, cols, depth, sms)
+@pytest.mark.parametrize("sms,tile_rows", [(74, 256), (66, 256), (148, 128), (7, 256)])
+def test_schedule_visits_each_tile_once(lib, kind, rows, cols, depth, sms, tile_rows):
+    info, counts = binding.kd_debug_schedule(kind, rows, cols, depth, sms, tile_rows)
     assert counts.min() == 1 and counts.max() == 1
     assert info["grid"] == min(sms, info["units"])
     if kind == 0:
@@ -116,12 +116,14 @@ def test_schedule_visits_each_tile_once(lib, kind, rows, cols, depth, sms):
 
 def test_forward_schedule_is_balanced_on_gptoss_shapes(lib):
     for N in (4096, 16384, 32768, 65536, 262144):
-        info, _ = binding.kd_debug_schedule(0, N, 201088, 2880, 148, with_counts=False)
+        info, _ = binding.kd_debug_schedule(0, N, 201088, 2880, 74, 256, with_counts=False)
+        assert info["units"] % 74 == 0, (N, info)
+        info, _ = binding.kd_debug_schedule(0, N, 201088, 2880, 148, 128, with_counts=False)
         assert info["units"] % 148 == 0, (N, info)
 
 
 def test_dh_split_fills_the_last_wave(lib):
-    info, _ = binding.kd_debug_schedule(1, 4096, 2880, 201088, 148, with_counts=False)
+    info, _ = binding.kd_debug_schedule(1, 4096, 2880, 201088, 74, 256, with_counts=False)
     units = info["units"]
     assert info["k_splits"] > 1
-    assert units / (-(-units // 148) * 148) > 0.95
+    assert units / (-(-units // 74) * 74) > 0.95

@@ -69,11 +69,11 @@ def lib() -> ctypes.CDLL:
         L.kd_get_status.restype = i32
         L.kd_status_string.argtypes = [i32]
         L.kd_status_string.restype = ctypes.c_char_p
-        L.kd_debug_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp]
+        L.kd_debug_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
         L.kd_debug_gemm_bf16.restype = i32
         L.kd_debug_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         L.kd_debug_wait_timeout.restype = i32
-        L.kd_debug_schedule.argtypes = [i32, i64, i64, i64, i32, vp, vp]
+        L.kd_debug_schedule.argtypes = [i32, i64, i64, i64, i32, i32, vp, vp]
         L.kd_debug_schedule.restype = i32
         L.kd_debug_profile.argtypes = [i32]
         L.kd_debug_profile.restype = i32
@@ -185,7 +185,7 @@ def kd_get_status(stream=None) -> int:
     return int(lib().kd_get_status(_stream(stream)))
 
 
-def kd_debug_gemm_bf16(A, B, C, a_mn: bool, b_mn: bool, stream=None):
+def kd_debug_gemm_bf16(A, B, C, a_mn: bool, b_mn: bool, cta_pair: bool = True, stream=None):
     """C = A·B^T through the tcgen05 mainloop (see kd_topk_kl_testing.h)."""
     if a_mn:
         K, M = A.shape
@@ -197,26 +197,29 @@ def kd_debug_gemm_bf16(A, B, C, a_mn: bool, b_mn: bool, stream=None):
     _ptr(B, torch.bfloat16, tuple(B.shape), "B", dev)
     _ptr(C, torch.float32, (M, N), "C", dev)
     _check(lib().kd_debug_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
-                                    int(a_mn), int(b_mn), _stream(stream)), "kd_debug_gemm_bf16")
+                                    int(a_mn), int(b_mn), int(cta_pair), _stream(stream)),
+           "kd_debug_gemm_bf16")
 
 
 def kd_debug_wait_timeout(timeout_ns: int, stream=None):
     _check(lib().kd_debug_wait_timeout(int(timeout_ns), _stream(stream)), "kd_debug_wait_timeout")
 
 
-def kd_debug_schedule(kind: int, rows: int, cols: int, depth: int, num_sms: int, with_counts=True):
+def kd_debug_schedule(kind: int, rows: int, cols: int, depth: int, grid_units: int,
+                      tile_rows: int = 256, with_counts=True):
     """Host-only: the work schedule as (info dict, per-(m, n, k-block) visit counts or None)."""
     import numpy as np
     info = np.zeros(8, dtype=np.int64)
-    code = lib().kd_debug_schedule(kind, rows, cols, depth, num_sms, None, info.ctypes.data)
+    code = lib().kd_debug_schedule(kind, rows, cols, depth, grid_units, tile_rows, None,
+                                   info.ctypes.data)
     _check(code, "kd_debug_schedule")
     counts = None
     if with_counts:
         MB, NB, KB = int(info[2]), int(info[3]), int(info[4])
         counts = np.zeros(MB * NB * KB, dtype=np.int32)
         info2 = np.zeros(8, dtype=np.int64)
-        _check(lib().kd_debug_schedule(kind, rows, cols, depth, num_sms, counts.ctypes.data,
-                                       info2.ctypes.data), "kd_debug_schedule")
+        _check(lib().kd_debug_schedule(kind, rows, cols, depth, grid_units, tile_rows,
+                                       counts.ctypes.data, info2.ctypes.data), "kd_debug_schedule")
         counts = counts.reshape(MB, NB, KB)
     keys = ["units", "grid", "MB", "NB", "KB", "BN", "max_slots", "k_splits"]
     return {k: int(v) for k, v in zip(keys, info)}, counts

@@ -32,14 +32,24 @@
 
 namespace kd {
 
-constexpr int kStages = 4;
-constexpr int kAStageBytes = kBM * kBK * 2;      // 16 KB
-constexpr int kBStageBytes = kBNMax * kBK * 2;   // 32 KB
-constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+// Per-CTA pipeline geometry. Single CTA: 128 x 256 tiles, 48 KB k-blocks, 4 stages.
+// CTA pair (cta_group::2): 256 x BN tiles; each CTA holds 128 rows of A and half
+// of B (<= 128 columns) per k-block, 32 KB, 6 stages.
+template <bool PAIR>
+struct Geo {
+  static constexpr int kTileRows = PAIR ? 256 : 128;
+  static constexpr int kBRows = PAIR ? 128 : 256;               // B rows (columns of D) per CTA
+  static constexpr int kAStageBytes = kBM * kBK * 2;              // 16 KB
+  static constexpr int kBStageBytes = kBRows * kBK * 2;           // 16 / 32 KB
+  static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+};
 constexpr int kSlabBytes = 64 * kBK * 2;         // one 64-wide MN slab of a k-block: 8 KB
 constexpr int kGemmThreads = 192;
 constexpr int kTmemCols = 512;
-constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kGemmSmemBytes = Geo<false>::kSmemBytes > Geo<true>::kSmemBytes ? Geo<false>::kSmemBytes
+                                                                               : Geo<true>::kSmemBytes;
 
 enum Epi : int { kEpiFwd = 0, kEpiDz = 1, kEpiDh = 2, kEpiDw = 3, kEpiPlain = 4 };
 
@@ -116,16 +126,17 @@ __device__ __forceinline__ void store8_f32(float* dst, const float* v, bool add)
   *reinterpret_cast<float4*>(dst + 4) = b;
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs args) {
+  using G = Geo<PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* empty_bar = full_bar + kStages;
-  uint64_t* acc_full = empty_bar + kStages;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStageBytes);
+  uint64_t* empty_bar = full_bar + G::kStages;
+  uint64_t* acc_full = empty_bar + G::kStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain_bar = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
@@ -134,15 +145,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Sched& sc = args.sched;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0 = the pair's MMA issuer
+  const int64_t unit0 = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+  const int64_t unit_step = PAIR ? (gridDim.x >> 1) : gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < G::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);  // one arrive per epilogue warp
+      mbar_init(&acc_empty[a], PAIR ? 8 : 4);  // one arrive per epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -151,73 +165,89 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<PAIR>(tmem_slot, kTmemCols);
+    tmem_relinquish<PAIR>();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // the peer's copies and arrives target barriers initialised above
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+
+  // Give up in this CTA and, for a pair, in the peer too.
+  auto raise_abort = [&]() {
+    *abort_flag = 1;
+    if constexpr (PAIR)
+      st_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u), 1u);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_mask = 0;         // stages loaded at least once
-      uint32_t last_parity = 0;         // parity of each stage's last load
       bool ok = true;
-      for (int64_t u = blockIdx.x; ok && u < sc.total; u += gridDim.x) {
+      for (int64_t u = unit0; ok && u < sc.total; u += unit_step) {
         const Unit d = sched_unit(sc, u);
-        const int m0 = d.m_blk * kBM;
+        const int m_rows = d.m_blk * G::kTileRows + static_cast<int>(rank) * kBM;  // this CTA's A rows
         for (int nb = d.n_begin; ok && nb < d.n_end; ++nb) {
-          const int n0 = nb * args.BN;
+          const int n_cols = nb * args.BN + (PAIR ? static_cast<int>(rank) * (args.BN / 2) : 0);
           for (int kb = d.kb_begin; kb < d.kb_end; ++kb) {
             if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, args.timeout_ns,
                                    args.status, 6)) {
               ok = false;
+              raise_abort();
               break;
             }
-            mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
-            uint8_t* a_dst = smem + stage * kStageBytes;
-            uint8_t* b_dst = a_dst + kAStageBytes;
+            uint8_t* a_dst = smem + stage * G::kStageBytes;
+            uint8_t* b_dst = a_dst + G::kAStageBytes;
             const int k0 = kb * kBK;
-            if (!A_MN) {
-              tma_load_2d(a_dst, &tmA, &full_bar[stage], k0, m0 + args.a_row_off);
+            if constexpr (PAIR) {
+              // both CTAs' copies complete on the first CTA's full barrier
+              const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0u);
+              if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * G::kStageBytes);
+              if (!A_MN) {
+                tma_load_2d_pair(a_dst, &tmA, fb, k0, m_rows + args.a_row_off);
+              } else {
+                tma_load_2d_pair(a_dst, &tmA, fb, m_rows, k0);
+                tma_load_2d_pair(a_dst + kSlabBytes, &tmA, fb, m_rows + 64, k0);
+              }
+              if (!B_MN) {
+                tma_load_2d_pair(b_dst, &tmB, fb, k0, n_cols);
+              } else {
+                tma_load_2d_pair(b_dst, &tmB, fb, n_cols, k0 + args.b_k_off);
+                tma_load_2d_pair(b_dst + kSlabBytes, &tmB, fb, n_cols + 64, k0 + args.b_k_off);
+              }
             } else {
-              tma_load_2d(a_dst, &tmA, &full_bar[stage], m0, k0);
-              tma_load_2d(a_dst + kSlabBytes, &tmA, &full_bar[stage], m0 + 64, k0);
-            }
-            if (!B_MN) {
-              tma_load_2d(b_dst, &tmB, &full_bar[stage], k0, n0);
-            } else {
+              mbar_arrive_expect_tx(&full_bar[stage], G::kStageBytes);
+              if (!A_MN) {
+                tma_load_2d(a_dst, &tmA, &full_bar[stage], k0, m_rows + args.a_row_off);
+              } else {
+                tma_load_2d(a_dst, &tmA, &full_bar[stage], m_rows, k0);
+                tma_load_2d(a_dst + kSlabBytes, &tmA, &full_bar[stage], m_rows + 64, k0);
+              }
+              if (!B_MN) {
+                tma_load_2d(b_dst, &tmB, &full_bar[stage], k0, n_cols);
+              } else {
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                tma_load_2d(b_dst + j * kSlabBytes, &tmB, &full_bar[stage], n0 + 64 * j,
-                            k0 + args.b_k_off);
+                for (int j = 0; j < 4; ++j)
+                  tma_load_2d(b_dst + j * kSlabBytes, &tmB, &full_bar[stage], n_cols + 64 * j,
+                              k0 + args.b_k_off);
+              }
             }
-            issued_mask |= 1u << stage;
-            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-            if (++stage == kStages) {
+            if (++stage == G::kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
         }
       }
-      if (!ok) {
-        // Leave no bulk copy in flight into this CTA's shared memory.
-        for (int s = 0; s < kStages; ++s)
-          if (issued_mask & (1u << s)) {
-            volatile int no_abort = 0;
-            mbar_wait_bounded(&full_bar[s], (last_parity >> s) & 1u, &no_abort, 100000000ull,
-                              args.status, 6);
-          }
-      }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (first CTA)
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -226,14 +256,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool any_mma = false;
       const uint32_t a_lbo = A_MN ? kSlabBytes : 16;
       const uint32_t b_lbo = B_MN ? kSlabBytes : 16;
-      const uint32_t a_kstep = A_MN ? 16 * 128 : 32;  // bytes per 16-wide k step
+      const uint32_t a_kstep = A_MN ? 16 * 128 : 32;  // bytes per 16-deep k step
       const uint32_t b_kstep = B_MN ? 16 * 128 : 32;
-      for (int64_t u = blockIdx.x; ok && u < sc.total; u += gridDim.x) {
+      for (int64_t u = unit0; ok && u < sc.total; u += unit_step) {
         const Unit d = sched_unit(sc, u);
         for (int nb = d.n_begin; ok && nb < d.n_end; ++nb) {
           if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, args.timeout_ns,
                                  args.status, 6)) {
             ok = false;
+            raise_abort();
             break;
           }
           tc_fence_after();
@@ -242,27 +273,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, args.timeout_ns,
                                    args.status, 6)) {
               ok = false;
+              raise_abort();
               break;
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
-            const uint32_t b_addr = a_addr + kAStageBytes;
+            const uint32_t a_addr = smem_u32(smem + stage * G::kStageBytes);
+            const uint32_t b_addr = a_addr + G::kAStageBytes;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
               const uint64_t adesc = umma_smem_desc(a_addr + k * a_kstep, a_lbo, 1024);
               const uint64_t bdesc = umma_smem_desc(b_addr + k * b_kstep, b_lbo, 1024);
-              umma_bf16(d_tmem, adesc, bdesc, args.idesc,
-                        (kb > d.kb_begin || k > 0) ? 1u : 0u);
+              umma_bf16<PAIR>(d_tmem, adesc, bdesc, args.idesc,
+                              (kb > d.kb_begin || k > 0) ? 1u : 0u);
             }
             any_mma = true;
-            umma_commit(&empty_bar[stage]);
-            if (++stage == kStages) {
+            umma_commit<PAIR>(&empty_bar[stage]);
+            if (++stage == G::kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          umma_commit(&acc_full[acc]);
+          umma_commit<PAIR>(&acc_full[acc]);
           if (++acc == 2) {
             acc = 0;
             acc_phase ^= 1u;
@@ -271,7 +303,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok && any_mma) {
         // Let every issued MMA finish before TMEM is released.
-        umma_commit(drain_bar);
+        umma_commit<PAIR>(drain_bar);
         volatile int no_abort = 0;
         mbar_wait_bounded(drain_bar, 0, &no_abort, 100000000ull, args.status, 6);
       }
@@ -279,15 +311,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM sub-partition this warp may read
-    const int row_in_tile = q * 32 + lane;
+    const int row_in_tile = static_cast<int>(rank) * kBM + q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t acc_empty_addr0 =
+        PAIR ? mapa_shared(smem_u32(&acc_empty[0]), 0u) : smem_u32(&acc_empty[0]);
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     const int K = args.K;
-    for (int64_t u = blockIdx.x; ok && u < sc.total; u += gridDim.x) {
+    for (int64_t u = unit0; ok && u < sc.total; u += unit_step) {
       const Unit d = sched_unit(sc, u);
-      const int m0 = d.m_blk * kBM;
+      const int m0 = d.m_blk * G::kTileRows;
       const int row = m0 + row_in_tile;          // local output row
       const bool row_ok = row < args.M;
       // per-unit state
@@ -318,6 +352,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                            args.status, 6);
         if (!__all_sync(0xffffffffu, got)) {  // keep the warp's decision uniform
           ok = false;
+          if (lane == 0) raise_abort();
           break;
         }
         tc_fence_after();
@@ -420,7 +455,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster(acc_empty_addr0 + 8u * static_cast<uint32_t>(acc));
+          else
+            mbar_arrive(&acc_empty[acc]);
+        }
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -431,10 +471,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
 
+  if (*abort_flag) {
+    // Bulk copies and MMAs already issued by this CTA or its peer complete within
+    // microseconds; give them a millisecond before shared memory and TMEM go away.
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) tmem_dealloc<PAIR>(tmem_base, kTmemCols);
 }
 
 }  // namespace kd

@@ -35,8 +35,13 @@ struct DevInfo {
   bool ready = false;
   bool ok = false;
   int num_sms = 0;
+  int pair_slots = 0;     // CTA pairs of the GEMM kernel that fit on the device at once
   int* status = nullptr;  // device address of g_kd_status
 };
+
+// Every GEMM of the loss runs on CTA pairs (cta_group::2, 256-row tiles).
+constexpr bool kPair = true;
+constexpr int kTileRows = Geo<kPair>::kTileRows;
 
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
@@ -106,6 +111,28 @@ const DevInfo* device_info(kd_status* err) {
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     d.ok = sym && g_encode != nullptr && major == 10 && minor == 3 && d.num_sms > 0;
+    d.pair_slots = d.num_sms / 2;
+    if (d.ok) {
+      auto kern = kd_gemm_kernel<kEpiPlain, false, false, true>;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes) ==
+          cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(d.num_sms & ~1));
+        cfg.blockDim = dim3(kGemmThreads);
+        cfg.dynamicSmemBytes = kGemmSmemBytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0 &&
+            n < d.pair_slots)
+          d.pair_slots = n;
+      }
+    }
     cudaGetLastError();
   }
   if (!d.ok) {
@@ -167,10 +194,10 @@ Layout plan(int64_t N, int D, int V, int K, int64_t chunk) {
   // backward (reuses the forward's region)
   off = common;
   int64_t C = chunk <= 0 ? 4096 : chunk;
-  C = cdiv(C, kBM) * kBM;
-  const int64_t Nr = cdiv(N, kBM) * kBM;
+  C = cdiv(C, kTileRows) * kTileRows;
+  const int64_t Nr = cdiv(N, kTileRows) * kTileRows;
   if (C > Nr) C = Nr;
-  if (C < kBM) C = kBM;
+  if (C < kTileRows) C = kTileRows;
   L.C = C;
   L.C_pad = C;
   L.dz_ld = static_cast<int64_t>(L.NB) * kBNMax;
@@ -193,12 +220,12 @@ int ksplit_that_fits(const Layout& L, int D, size_t ws_bytes, int wanted) {
   return fit < wanted ? fit : wanted;
 }
 
-int wanted_ksplit(int64_t C_pad, int D, int V, int num_sms) {
-  const int MB = static_cast<int>(C_pad / kBM);
+int wanted_ksplit(int64_t C_pad, int D, int V, int grid) {
+  const int MB = static_cast<int>(C_pad / kTileRows);
   const int bn = hidden_tile_width(D);
   const int NBd = static_cast<int>(cdiv(D, bn));
   const int KB = static_cast<int>(cdiv(V, kBK));
-  return choose_ksplit(static_cast<int64_t>(MB) * NBd, KB, num_sms);
+  return choose_ksplit(static_cast<int64_t>(MB) * NBd, KB, grid);
 }
 
 kd_status cuda_check() {
@@ -206,20 +233,39 @@ kd_status cuda_check() {
   return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
-template <int EPI, bool AMN, bool BMN>
-kd_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int num_sms,
-                      cudaStream_t s) {
-  auto kern = kd_gemm_kernel<EPI, AMN, BMN>;
+template <int EPI, bool AMN, bool BMN, bool PAIR>
+kd_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
+                      const DevInfo* di, cudaStream_t s) {
+  auto kern = kd_gemm_kernel<EPI, AMN, BMN, PAIR>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes) !=
       cudaSuccess) {
     cudaGetLastError();
     return KD_ERR_CUDA;
   }
-  int64_t grid = args.sched.total < num_sms ? args.sched.total : num_sms;
-  if (grid < 1) return KD_OK;
-  kern<<<static_cast<unsigned>(grid), kGemmThreads, kGemmSmemBytes, s>>>(a, b, args);
+  const int64_t slots = PAIR ? di->pair_slots : di->num_sms;
+  const int64_t units = args.sched.total < slots ? args.sched.total : slots;
+  if (units < 1) return KD_OK;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * units : units));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a, b, args) != cudaSuccess) {
+    cudaGetLastError();
+    return KD_ERR_CUDA;
+  }
   return cuda_check();
 }
+
+// Persistent workers the GEMM schedules are planned for (CTA pairs).
+inline int gemm_slots(const DevInfo* di) { return kPair ? di->pair_slots : di->num_sms; }
 
 GemmArgs base_args(const DevInfo* di) {
   GemmArgs a;
@@ -257,7 +303,7 @@ extern "C" size_t kd_topk_kl_workspace_size(int64_t N, int D, int V, int K, int6
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) sms = n;
   }
   cudaGetLastError();
-  const int ks = wanted_ksplit(L.C_pad, D, V, sms);
+  const int ks = wanted_ksplit(L.C_pad, D, V, kPair ? sms / 2 : sms);
   size_t bwd = L.bwd_end;
   if (ks > 1) bwd = align256(L.dhp + static_cast<size_t>(ks) * L.C_pad * D * sizeof(float));
   return L.fwd_end > bwd ? L.fwd_end : bwd;
@@ -296,16 +342,16 @@ extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const 
 
   CUtensorMap mH, mW;
   if (!make_map(&mH, H, D, N, static_cast<uint64_t>(D) * 2, kBK, kBM) ||
-      !make_map(&mW, W, D, V, static_cast<uint64_t>(D) * 2, kBK, kBNMax))
+      !make_map(&mW, W, D, V, static_cast<uint64_t>(D) * 2, kBK, Geo<kPair>::kBRows))
     return KD_ERR_CUDA;
-  const int MB = static_cast<int>(cdiv(N, kBM));
+  const int MB = static_cast<int>(cdiv(N, kTileRows));
   const int KB = static_cast<int>(cdiv(D, kBK));
   GemmArgs a = base_args(di);
-  a.sched = make_panel_sched(MB, L.NB, KB, di->num_sms);
+  a.sched = make_panel_sched(MB, L.NB, KB, gemm_slots(di));
   a.M = static_cast<int>(N);
   a.Ncols = V;
   a.BN = kBNMax;
-  a.idesc = umma_idesc_bf16(kBM, kBNMax, false, false);
+  a.idesc = umma_idesc_bf16(kTileRows, kBNMax, false, false);
   a.K = K;
   a.scale2 = 1.4426950408889634f * inv_T;
   a.inv_T = inv_T;
@@ -315,12 +361,12 @@ extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const 
   a.slots = L.slots;
   {
     ProfScope ps(kProfFwdGemm, s);
-    if ((st = launch_gemm<kEpiFwd, false, false>(mH, mW, a, di->num_sms, s)) != KD_OK) return st;
+    if ((st = launch_gemm<kEpiFwd, false, false, kPair>(mH, mW, a, di, s)) != KD_OK) return st;
   }
   {
     ProfScope ps(kProfCombine, s);
     kd_combine_kernel<<<static_cast<unsigned>(cdiv(N, 256)), 256, 0, s>>>(
-        a.sched, part, L.slots, pairs, zk, ent, mask, N, K, V, inv_T, loss, lse);
+        a.sched, kTileRows, part, L.slots, pairs, zk, ent, mask, N, K, V, inv_T, loss, lse);
   }
   return cuda_check();
 }
@@ -346,7 +392,7 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
   }
   const Layout L = plan(N, D, V, K, chunk_tokens);
   if (ws_bytes < L.bwd_end) return KD_ERR_WORKSPACE;
-  const int KS = ksplit_that_fits(L, D, ws_bytes, wanted_ksplit(L.C_pad, D, V, di->num_sms));
+  const int KS = ksplit_that_fits(L, D, ws_bytes, wanted_ksplit(L.C_pad, D, V, gemm_slots(di)));
   uint8_t* w = static_cast<uint8_t*>(ws);
   int2* pairs = reinterpret_cast<int2*>(w + L.pairs);
   float* ent = reinterpret_cast<float*>(w + L.ent);
@@ -366,7 +412,8 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
   CUtensorMap mH_k, mW_k, mDz_k, mW_mn, mDz_mn, mH_mn;
   const uint64_t rowH = static_cast<uint64_t>(D) * 2;
   const uint64_t rowDz = static_cast<uint64_t>(L.dz_ld) * 2;
-  if (!make_map(&mH_k, H, D, N, rowH, kBK, kBM) || !make_map(&mW_k, W, D, V, rowH, kBK, kBNMax) ||
+  if (!make_map(&mH_k, H, D, N, rowH, kBK, kBM) ||
+      !make_map(&mW_k, W, D, V, rowH, kBK, Geo<kPair>::kBRows) ||
       !make_map(&mDz_k, dz, V, L.C_pad, rowDz, kBK, kBM) ||
       !make_map(&mW_mn, W, D, V, rowH, 64, kBK) || !make_map(&mDz_mn, dz, V, L.C_pad, rowDz, 64, kBK) ||
       !make_map(&mH_mn, H, D, N, rowH, 64, kBK))
@@ -374,18 +421,18 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
 
   const int KBd = static_cast<int>(cdiv(D, kBK));
   const int KBv = static_cast<int>(cdiv(V, kBK));
-  const int MBv = static_cast<int>(cdiv(V, kBM));
+  const int MBv = static_cast<int>(cdiv(V, kTileRows));
   for (int64_t c0 = 0; c0 < N; c0 += L.C) {
     const int64_t rows = (N - c0) < L.C ? (N - c0) : L.C;
-    const int MBc = static_cast<int>(cdiv(rows, kBM));
+    const int MBc = static_cast<int>(cdiv(rows, kTileRows));
 
     // 1. recompute the chunk's logits, dZ epilogue -> dz (bf16)
     GemmArgs a = base_args(di);
-    a.sched = make_panel_sched(MBc, L.NB, KBd, di->num_sms);
+    a.sched = make_panel_sched(MBc, L.NB, KBd, gemm_slots(di));
     a.M = static_cast<int>(rows);
     a.Ncols = V;
     a.BN = kBNMax;
-    a.idesc = umma_idesc_bf16(kBM, kBNMax, false, false);
+    a.idesc = umma_idesc_bf16(kTileRows, kBNMax, false, false);
     a.a_row_off = static_cast<int>(c0);
     a.row_base = c0;
     a.K = K;
@@ -399,7 +446,7 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     a.dz_ld = L.dz_ld;
     {
       ProfScope ps(kProfDzGemm, s);
-      if ((st = launch_gemm<kEpiDz, false, false>(mH_k, mW_k, a, di->num_sms, s)) != KD_OK) return st;
+      if ((st = launch_gemm<kEpiDz, false, false, kPair>(mH_k, mW_k, a, di, s)) != KD_OK) return st;
     }
 
     // 2. dH rows of the chunk = dZ W (contraction over V, split KS ways)
@@ -408,14 +455,14 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     h.M = static_cast<int>(rows);
     h.Ncols = D;
     h.BN = BNd;
-    h.idesc = umma_idesc_bf16(kBM, BNd, false, true);
+    h.idesc = umma_idesc_bf16(kTileRows, BNd, false, true);
     h.row_base = c0;
     h.out_bf16 = dH;
     h.out_f32 = dhp;
     h.part_stride = L.C_pad * static_cast<int64_t>(D);
     {
       ProfScope ps(kProfDhGemm, s);
-      if ((st = launch_gemm<kEpiDh, false, true>(mDz_k, mW_mn, h, di->num_sms, s)) != KD_OK) return st;
+      if ((st = launch_gemm<kEpiDh, false, true, kPair>(mDz_k, mW_mn, h, di, s)) != KD_OK) return st;
     }
     if (h.sched.KS > 1) {
       const int64_t groups = rows * (D / 8);
@@ -433,14 +480,14 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     g.M = V;
     g.Ncols = D;
     g.BN = BNd;
-    g.idesc = umma_idesc_bf16(kBM, BNd, true, true);
+    g.idesc = umma_idesc_bf16(kTileRows, BNd, true, true);
     g.b_k_off = static_cast<int>(c0);
     g.out_f32 = dW;
     g.ld_out = D;
     g.accumulate = (c0 > 0 || accumulate_dW) ? 1 : 0;
     {
       ProfScope ps(kProfDwGemm, s);
-      if ((st = launch_gemm<kEpiDw, true, true>(mDz_mn, mH_mn, g, di->num_sms, s)) != KD_OK) return st;
+      if ((st = launch_gemm<kEpiDw, true, true, kPair>(mDz_mn, mH_mn, g, di, s)) != KD_OK) return st;
     }
   }
   return KD_OK;
@@ -478,7 +525,7 @@ extern "C" const char* kd_status_string(kd_status status) {
 // ------------------------------------------------------------------ test hooks
 
 extern "C" kd_status kd_debug_gemm_bf16(const uint16_t* A, const uint16_t* B, float* C, int M, int N,
-                                        int K, int a_mn, int b_mn, kd_stream_t stream) {
+                                        int K, int a_mn, int b_mn, int cta_pair, kd_stream_t stream) {
   if (M <= 0 || N <= 0 || K <= 0 || M % 8 || N % 8 || K % 8) return KD_ERR_ARG;
   if (!A || !B || !C) return KD_ERR_ARG;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return KD_ERR_ALIGN;
@@ -487,6 +534,9 @@ extern "C" kd_status kd_debug_gemm_bf16(const uint16_t* A, const uint16_t* B, fl
   const DevInfo* di = device_info(&st);
   if (!di) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool pair = cta_pair != 0;
+  const int rows = pair ? Geo<true>::kTileRows : Geo<false>::kTileRows;
+  const int b_rows = pair ? Geo<true>::kBRows : Geo<false>::kBRows;
   const int BN = b_mn ? hidden_tile_width(N) : kBNMax;
   CUtensorMap ma, mb;
   bool ok;
@@ -495,22 +545,27 @@ extern "C" kd_status kd_debug_gemm_bf16(const uint16_t* A, const uint16_t* B, fl
   else
     ok = make_map(&ma, A, M, K, static_cast<uint64_t>(M) * 2, 64, kBK);
   if (!b_mn)
-    ok = ok && make_map(&mb, B, K, N, static_cast<uint64_t>(K) * 2, kBK, kBNMax);
+    ok = ok && make_map(&mb, B, K, N, static_cast<uint64_t>(K) * 2, kBK, b_rows);
   else
     ok = ok && make_map(&mb, B, N, K, static_cast<uint64_t>(N) * 2, 64, kBK);
   if (!ok) return KD_ERR_CUDA;
   GemmArgs a = base_args(di);
-  a.sched = make_tile_sched(static_cast<int>(cdiv(M, kBM)), static_cast<int>(cdiv(N, BN)),
+  a.sched = make_tile_sched(static_cast<int>(cdiv(M, rows)), static_cast<int>(cdiv(N, BN)),
                             static_cast<int>(cdiv(K, kBK)), 1);
   a.M = M;
   a.Ncols = N;
   a.BN = BN;
-  a.idesc = umma_idesc_bf16(kBM, BN, a_mn != 0, b_mn != 0);
+  a.idesc = umma_idesc_bf16(rows, BN, a_mn != 0, b_mn != 0);
   a.out_f32 = C;
   a.ld_out = N;
-  if (!a_mn && !b_mn) return launch_gemm<kEpiPlain, false, false>(ma, mb, a, di->num_sms, s);
-  if (!a_mn && b_mn) return launch_gemm<kEpiPlain, false, true>(ma, mb, a, di->num_sms, s);
-  return launch_gemm<kEpiPlain, true, true>(ma, mb, a, di->num_sms, s);
+  if (pair) {
+    if (!a_mn && !b_mn) return launch_gemm<kEpiPlain, false, false, true>(ma, mb, a, di, s);
+    if (!a_mn && b_mn) return launch_gemm<kEpiPlain, false, true, true>(ma, mb, a, di, s);
+    return launch_gemm<kEpiPlain, true, true, true>(ma, mb, a, di, s);
+  }
+  if (!a_mn && !b_mn) return launch_gemm<kEpiPlain, false, false, false>(ma, mb, a, di, s);
+  if (!a_mn && b_mn) return launch_gemm<kEpiPlain, false, true, false>(ma, mb, a, di, s);
+  return launch_gemm<kEpiPlain, true, true, false>(ma, mb, a, di, s);
 }
 
 extern "C" kd_status kd_debug_wait_timeout(uint64_t timeout_ns, kd_stream_t stream) {
@@ -523,10 +578,12 @@ extern "C" kd_status kd_debug_wait_timeout(uint64_t timeout_ns, kd_stream_t stre
 }
 
 extern "C" kd_status kd_debug_schedule(int kind, int64_t rows, int64_t cols, int64_t depth,
-                                       int num_sms, int32_t* counts, int64_t* info) {
-  if (rows <= 0 || cols <= 0 || depth <= 0 || num_sms <= 0 || kind < 0 || kind > 2 || !info)
+                                       int grid_units, int tile_rows, int32_t* counts, int64_t* info) {
+  if (rows <= 0 || cols <= 0 || depth <= 0 || grid_units <= 0 || kind < 0 || kind > 2 || !info ||
+      (tile_rows != 128 && tile_rows != 256))
     return KD_ERR_ARG;
-  const int MB = static_cast<int>(cdiv(rows, kBM));
+  const int num_sms = grid_units;
+  const int MB = static_cast<int>(cdiv(rows, tile_rows));
   const int KB = static_cast<int>(cdiv(depth, kBK));
   int BN, NB;
   Sched sc;
