@@ -164,9 +164,12 @@ def oracle_rate(p, seconds: float, seed: int = 0, max_rows: int = 1024):
         oracle.kd_backward(Hs, W64, idx[rows], t[rows], m[rows], p.T, g)
         return len(rows), time.perf_counter() - t0
 
-    n0, s0 = run(8)
-    n = int(min(max_rows, max(8, 8 * seconds / max(s0, 1e-3))))
-    n1, s1 = run(n)
+    run(8)                       # first call pays BLAS start-up; not timed
+    n1, s1 = 0, 0.0
+    while s1 < seconds and n1 < max_rows:   # batches of 16 rows until the time target
+        n, s = run(16)
+        n1 += n
+        s1 += s
     try:
         from threadpoolctl import threadpool_info
         threads = max(int(d.get("num_threads", 1)) for d in threadpool_info()) or os.cpu_count()

@@ -16,6 +16,9 @@
 //   kEpiDh    dH tile (bf16, or fp32 partial per k-split)
 //   kEpiDw    dW tile, stored or added to the existing fp32 values
 //   kEpiPlain fp32 C tile (mainloop test hook)
+// fp32 tiles (dW, plain, dH partials) are staged per warp in shared memory as
+// 32 x 16 boxes and written by TMA: a bulk-tensor store, or for an accumulating
+// dW a bulk-tensor add that L2 applies (one owner per tile, so no atomics race).
 //
 // Operand layouts in shared memory are the TMA 128-byte-swizzled boxes: a
 // K-major operand is rows x 64 bf16 (one 128-byte line per row); an MN-major
@@ -32,6 +35,14 @@
 
 namespace kd {
 
+// fp32 output boxes staged in shared memory for the TMA store / reduce epilogue:
+// 32 rows x 16 columns (64 bytes a row, 64-byte swizzle), two boxes per 32-column
+// TMEM chunk, two chunks in flight per epilogue warp.
+constexpr int kOutBoxCols = 16;
+constexpr int kOutBoxBytes = 32 * kOutBoxCols * 4;       // 2 KB
+constexpr int kOutChunkBytes = 2 * kOutBoxBytes;          // 4 KB: one 32-column chunk
+constexpr int kStagingBytes = 4 * 2 * kOutChunkBytes;     // 4 warps x 2 chunks = 32 KB
+
 // Per-CTA pipeline geometry. Single CTA: 128 x 256 tiles, 48 KB k-blocks, 4 stages.
 // CTA pair (cta_group::2): 256 x BN tiles; each CTA holds 128 rows of A and half
 // of B (<= 128 columns) per k-block, 32 KB, 6 stages.
@@ -43,7 +54,8 @@ struct Geo {
   static constexpr int kBStageBytes = kBRows * kBK * 2;           // 16 / 32 KB
   static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
   static constexpr int kStages = PAIR ? 6 : 4;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kRingBytes + kStagingBytes + 1024 /*align*/ + 256 /*barriers*/;
 };
 constexpr int kSlabBytes = 64 * kBK * 2;         // one 64-wide MN slab of a k-block: 8 KB
 constexpr int kGemmThreads = 192;
@@ -79,9 +91,48 @@ struct GemmArgs {
   int64_t part_stride;  // dh: elements per k-split slice
   uint16_t* out_bf16;   // dH
   int accumulate;       // dW: add to existing values
+  int out_slot_rows;    // dh partials: rows of one k-split slice in the tmC tensor
   int* status;
   uint64_t timeout_ns;
 };
+
+// fp32 tiles leave through tmC (TMA store, or TMA add for an accumulating dW):
+// dW, the plain GEMM, and the dH k-split partials.
+template <int EPI>
+__host__ __device__ __forceinline__ bool uses_tma_out(const GemmArgs& a) {
+  return EPI == kEpiDw || EPI == kEpiPlain || (EPI == kEpiDh && a.sched.KS > 1);
+}
+
+// One 32-column TMEM chunk of a warp's 32 rows -> two swizzled 32 x 16 fp32 boxes
+// in shared memory -> TMA store or add at (x0, y0). Lane r holds row r. The
+// 64-byte swizzle puts 16-byte piece j of row r at piece j ^ ((r >> 1) & 3),
+// which is what the tensor map's SWIZZLE_64B expects and keeps the eight
+// lanes of each 128-bit store phase on distinct banks.
+__device__ __forceinline__ void send_chunk(const CUtensorMap* map, uint8_t* buf, const float (&v)[32],
+                                           int lane, int x0, int y0, int boxes, bool add) {
+  const uint32_t base = smem_u32(buf) + static_cast<uint32_t>(lane) * 64u;
+  const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t addr = base + b * kOutBoxBytes + ((static_cast<uint32_t>(j) ^ sw) << 4);
+      st_shared_v4(addr, v[16 * b + 4 * j + 0], v[16 * b + 4 * j + 1], v[16 * b + 4 * j + 2],
+                   v[16 * b + 4 * j + 3]);
+    }
+  }
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    for (int b = 0; b < boxes; ++b) {
+      if (add)
+        tma_reduce_add_2d(map, buf + b * kOutBoxBytes, x0 + kOutBoxCols * b, y0);
+      else
+        tma_store_2d(map, buf + b * kOutBoxBytes, x0 + kOutBoxCols * b, y0);
+    }
+    bulk_commit_group();
+  }
+}
 
 __device__ __forceinline__ float select32(const float (&v)[32], int j) {
   float r = v[0];
@@ -112,29 +163,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Store 8 fp32 (32 bytes) or add them to what is there.
-__device__ __forceinline__ void store8_f32(float* dst, const float* v, bool add) {
-  float4 a = make_float4(v[0], v[1], v[2], v[3]);
-  float4 b = make_float4(v[4], v[5], v[6], v[7]);
-  if (add) {
-    const float4 oa = *reinterpret_cast<const float4*>(dst);
-    const float4 ob = *reinterpret_cast<const float4*>(dst + 4);
-    a.x += oa.x; a.y += oa.y; a.z += oa.z; a.w += oa.w;
-    b.x += ob.x; b.y += ob.y; b.z += ob.z; b.w += ob.w;
-  }
-  *reinterpret_cast<float4*>(dst) = a;
-  *reinterpret_cast<float4*>(dst + 4) = b;
-}
-
 template <int EPI, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   using G = Geo<PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStageBytes);
+  uint8_t* staging = smem + G::kRingBytes;  // 1024-byte aligned
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + kStagingBytes);
   uint64_t* empty_bar = full_bar + G::kStages;
   uint64_t* acc_full = empty_bar + G::kStages;
   uint64_t* acc_empty = acc_full + 2;
@@ -163,6 +201,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (uses_tma_out<EPI>(args)) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc<PAIR>(tmem_slot, kTmemCols);
@@ -319,6 +358,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     const int K = args.K;
+    const bool tma_out = uses_tma_out<EPI>(args);
+    uint8_t* my_staging = staging + q * 2 * kOutChunkBytes;
+    int sent = 0;  // chunks sent through TMA by this warp (selects the staging buffer)
     for (int64_t u = unit0; ok && u < sc.total; u += unit_step) {
       const Unit d = sched_unit(sc, u);
       const int m0 = d.m_blk * G::kTileRows;
@@ -420,35 +462,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               w.w = pack_bf16x2(dv[8 * g + 6], dv[8 * g + 7]);
               dst[g] = w;
             }
+          } else if (tma_out) {
+            // dW, plain C, dH k-split partials: staged boxes, TMA store / add.
+            // Boxes that start past the last row or column are not sent; the TMA
+            // unit clips the rest at the tensor's edges.
+            const int r0 = m0 + static_cast<int>(rank) * kBM + q * 32;  // warp-uniform
+            const int rem = args.BN - 32 * c;  // columns of this tile left (multiple of 16)
+            const int boxes = (rem >= 32 && col0 + kOutBoxCols < args.Ncols) ? 2 : 1;
+            if (r0 < args.M) {
+              const int y0 = (EPI == kEpiDh) ? r0 + d.slot * args.out_slot_rows : r0;
+              if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous boxes are read
+              __syncwarp();
+              send_chunk(&tmC, my_staging + (sent & 1) * kOutChunkBytes, v, lane, col0, y0, boxes,
+                         EPI == kEpiDw && args.accumulate != 0);
+              ++sent;
+            }
           } else if constexpr (EPI == kEpiDh) {
             if (row_ok) {
 #pragma unroll
               for (int g = 0; g < 4; ++g) {
                 const int cg = col0 + 8 * g;
                 if (32 * c + 8 * g < args.BN && cg < args.Ncols) {
-                  if (args.sched.KS == 1) {
-                    uint4 w;
-                    w.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
-                    w.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
-                    w.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
-                    w.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
-                    *reinterpret_cast<uint4*>(args.out_bf16 + (args.row_base + row) * args.Ncols + cg) = w;
-                  } else {
-                    store8_f32(args.out_f32 + d.slot * args.part_stride +
-                                   static_cast<int64_t>(row) * args.Ncols + cg,
-                               &v[8 * g], false);
-                  }
+                  uint4 w;
+                  w.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
+                  w.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
+                  w.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
+                  w.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
+                  *reinterpret_cast<uint4*>(args.out_bf16 + (args.row_base + row) * args.Ncols + cg) = w;
                 }
-              }
-            }
-          } else {  // kEpiDw, kEpiPlain
-            if (row_ok) {
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                const int cg = col0 + 8 * g;
-                if (32 * c + 8 * g < args.BN && cg < args.Ncols)
-                  store8_f32(args.out_f32 + static_cast<int64_t>(row) * args.ld_out + cg, &v[8 * g],
-                             EPI == kEpiDw && args.accumulate != 0);
               }
             }
           }
@@ -469,6 +510,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (EPI == kEpiFwd && ok && row_ok)
         args.part[static_cast<int64_t>(row) * args.slots + d.slot] = make_float2(m2, s2);
     }
+    // The output boxes must be fully written before the kernel ends (and before
+    // the staging memory is released).
+    if (tma_out && lane == 0) bulk_wait_group_all();
   }
 
   if (*abort_flag) {

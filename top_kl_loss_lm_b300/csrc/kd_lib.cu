@@ -158,6 +158,19 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D fp32 output map for the TMA store / add epilogue: `cols` contiguous
+// elements per row, `rows` rows, boxes of 16 x 32 with 64-byte swizzle.
+bool make_out_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kOutBoxCols), 32};
+  cuuint32_t es[2] = {1, 1};
+  std::memset(m, 0, sizeof(*m));
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -234,8 +247,8 @@ kd_status cuda_check() {
 }
 
 template <int EPI, bool AMN, bool BMN, bool PAIR>
-kd_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
-                      const DevInfo* di, cudaStream_t s) {
+kd_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                      const GemmArgs& args, const DevInfo* di, cudaStream_t s) {
   auto kern = kd_gemm_kernel<EPI, AMN, BMN, PAIR>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes) !=
       cudaSuccess) {
@@ -257,7 +270,7 @@ kd_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a, b, args) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, a, b, c, args) != cudaSuccess) {
     cudaGetLastError();
     return KD_ERR_CUDA;
   }
@@ -361,7 +374,7 @@ extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const 
   a.slots = L.slots;
   {
     ProfScope ps(kProfFwdGemm, s);
-    if ((st = launch_gemm<kEpiFwd, false, false, kPair>(mH, mW, a, di, s)) != KD_OK) return st;
+    if ((st = launch_gemm<kEpiFwd, false, false, kPair>(mH, mW, mH, a, di, s)) != KD_OK) return st;
   }
   {
     ProfScope ps(kProfCombine, s);
@@ -418,6 +431,12 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
       !make_map(&mW_mn, W, D, V, rowH, 64, kBK) || !make_map(&mDz_mn, dz, V, L.C_pad, rowDz, 64, kBK) ||
       !make_map(&mH_mn, H, D, N, rowH, 64, kBK))
     return KD_ERR_CUDA;
+  CUtensorMap mDw_out, mDhp_out;
+  if (!make_out_map(&mDw_out, dW, D, V, static_cast<uint64_t>(D) * 4) ||
+      (KS > 1 && !make_out_map(&mDhp_out, dhp, D, static_cast<uint64_t>(KS) * L.C_pad,
+                               static_cast<uint64_t>(D) * 4)))
+    return KD_ERR_CUDA;
+  if (KS <= 1) mDhp_out = mDw_out;  // unused: dH is written in bf16 directly
 
   const int KBd = static_cast<int>(cdiv(D, kBK));
   const int KBv = static_cast<int>(cdiv(V, kBK));
@@ -446,7 +465,8 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     a.dz_ld = L.dz_ld;
     {
       ProfScope ps(kProfDzGemm, s);
-      if ((st = launch_gemm<kEpiDz, false, false, kPair>(mH_k, mW_k, a, di, s)) != KD_OK) return st;
+      if ((st = launch_gemm<kEpiDz, false, false, kPair>(mH_k, mW_k, mH_k, a, di, s)) != KD_OK)
+        return st;
     }
 
     // 2. dH rows of the chunk = dZ W (contraction over V, split KS ways)
@@ -460,9 +480,11 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     h.out_bf16 = dH;
     h.out_f32 = dhp;
     h.part_stride = L.C_pad * static_cast<int64_t>(D);
+    h.out_slot_rows = static_cast<int>(L.C_pad);
     {
       ProfScope ps(kProfDhGemm, s);
-      if ((st = launch_gemm<kEpiDh, false, true, kPair>(mDz_k, mW_mn, h, di, s)) != KD_OK) return st;
+      if ((st = launch_gemm<kEpiDh, false, true, kPair>(mDz_k, mW_mn, mDhp_out, h, di, s)) != KD_OK)
+        return st;
     }
     if (h.sched.KS > 1) {
       const int64_t groups = rows * (D / 8);
@@ -487,7 +509,8 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     g.accumulate = (c0 > 0 || accumulate_dW) ? 1 : 0;
     {
       ProfScope ps(kProfDwGemm, s);
-      if ((st = launch_gemm<kEpiDw, true, true, kPair>(mDz_mn, mH_mn, g, di, s)) != KD_OK) return st;
+      if ((st = launch_gemm<kEpiDw, true, true, kPair>(mDz_mn, mH_mn, mDw_out, g, di, s)) != KD_OK)
+        return st;
     }
   }
   return KD_OK;
@@ -548,6 +571,8 @@ extern "C" kd_status kd_debug_gemm_bf16(const uint16_t* A, const uint16_t* B, fl
     ok = ok && make_map(&mb, B, K, N, static_cast<uint64_t>(K) * 2, kBK, b_rows);
   else
     ok = ok && make_map(&mb, B, N, K, static_cast<uint64_t>(N) * 2, 64, kBK);
+  CUtensorMap mc;
+  ok = ok && make_out_map(&mc, C, N, M, static_cast<uint64_t>(N) * 4);
   if (!ok) return KD_ERR_CUDA;
   GemmArgs a = base_args(di);
   a.sched = make_tile_sched(static_cast<int>(cdiv(M, rows)), static_cast<int>(cdiv(N, BN)),
@@ -559,13 +584,13 @@ extern "C" kd_status kd_debug_gemm_bf16(const uint16_t* A, const uint16_t* B, fl
   a.out_f32 = C;
   a.ld_out = N;
   if (pair) {
-    if (!a_mn && !b_mn) return launch_gemm<kEpiPlain, false, false, true>(ma, mb, a, di, s);
-    if (!a_mn && b_mn) return launch_gemm<kEpiPlain, false, true, true>(ma, mb, a, di, s);
-    return launch_gemm<kEpiPlain, true, true, true>(ma, mb, a, di, s);
+    if (!a_mn && !b_mn) return launch_gemm<kEpiPlain, false, false, true>(ma, mb, mc, a, di, s);
+    if (!a_mn && b_mn) return launch_gemm<kEpiPlain, false, true, true>(ma, mb, mc, a, di, s);
+    return launch_gemm<kEpiPlain, true, true, true>(ma, mb, mc, a, di, s);
   }
-  if (!a_mn && !b_mn) return launch_gemm<kEpiPlain, false, false, false>(ma, mb, a, di, s);
-  if (!a_mn && b_mn) return launch_gemm<kEpiPlain, false, true, false>(ma, mb, a, di, s);
-  return launch_gemm<kEpiPlain, true, true, false>(ma, mb, a, di, s);
+  if (!a_mn && !b_mn) return launch_gemm<kEpiPlain, false, false, false>(ma, mb, mc, a, di, s);
+  if (!a_mn && b_mn) return launch_gemm<kEpiPlain, false, true, false>(ma, mb, mc, a, di, s);
+  return launch_gemm<kEpiPlain, true, true, false>(ma, mb, mc, a, di, s);
 }
 
 extern "C" kd_status kd_debug_wait_timeout(uint64_t timeout_ns, kd_stream_t stream) {
