@@ -132,6 +132,22 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """Largest elapsed time over the ranks (one float64 all-reduce; identity at world 1)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_rate(units_per_rank: int, world: int, steps: int, ms: float) -> float:
+    """Whole-job rate: units every rank processed over the slowest rank's time."""
+    return world * units_per_rank * steps / (ms / 1000.0)
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -312,12 +328,9 @@ def run_ours(args, rank, world, local):
     if st != 0:
         raise RuntimeError(f"device status {binding.STATUS.get(st, st)} in the timed region")
     peak_mem = torch.cuda.max_memory_allocated()
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * N * args.steps / (ms / 1000.0)
-    tflops = world * flops_step * args.steps / (ms / 1000.0) / 1e12
+    ms = max_over_ranks(ms, world, dev)
+    value = job_rate(N, world, args.steps, ms)
+    tflops = job_rate(flops_step, world, args.steps, ms) / 1e12
 
     # ------------------------------------------------ end to end from host buffers
     e2e = None
@@ -355,14 +368,10 @@ def run_ours(args, rank, world, local):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([ems], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
+        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
         h2d = sum(x.numel() * x.element_size() for x in (hH, hidx, ht, hm, hg))
         d2h = hloss.numel() * 4 + 8
-        e2e = {"value": world * N * args.steps / (ems / 1000.0), "unit": "tokens/s",
+        e2e = {"value": job_rate(N, world, args.steps, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "note": "H, teacher ids/logits, mask and upstream grad copied from pinned host memory "
                        "each step; per-row loss and n_valid read back; W, dH, dW stay resident"}

@@ -12,7 +12,7 @@
 //             (partial per row and split) + gather of Z at the row's sorted
 //             teacher ids that fall in the tile
 //   kEpiDz    dZ = (g/T)(exp(Z/T - lse) - P~) with P~ scattered from the sorted
-//             ids, rounded to bf16 into the chunk's dZ buffer
+//             ids, rounded to bf16 and stored into the chunk's dZ buffer by TMA
 //   kEpiDh    dH tile (bf16, or fp32 partial per k-split)
 //   kEpiDw    dW tile, stored or added to the existing fp32 values
 //   kEpiPlain fp32 C tile (mainloop test hook)
@@ -100,7 +100,7 @@ struct GemmArgs {
 // dW, the plain GEMM, and the dH k-split partials.
 template <int EPI>
 __host__ __device__ __forceinline__ bool uses_tma_out(const GemmArgs& a) {
-  return EPI == kEpiDw || EPI == kEpiPlain || (EPI == kEpiDh && a.sched.KS > 1);
+  return EPI == kEpiDz || EPI == kEpiDw || EPI == kEpiPlain || (EPI == kEpiDh && a.sched.KS > 1);
 }
 
 // One 32-column TMEM chunk of a warp's 32 rows -> two swizzled 32 x 16 fp32 boxes
@@ -161,6 +161,26 @@ __device__ __forceinline__ int lower_bound_id(const int2* p, int K, int target) 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// bf16 variant for the dZ chunk: 32 rows x 32 columns rounded to bf16 (64 bytes
+// a row, same 64-byte swizzle), one TMA store at (x0, y0).
+__device__ __forceinline__ void send_chunk_bf16(const CUtensorMap* map, uint8_t* buf,
+                                                const float (&v)[32], int lane, int x0, int y0) {
+  const uint32_t base = smem_u32(buf) + static_cast<uint32_t>(lane) * 64u;
+  const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t addr = base + ((static_cast<uint32_t>(j) ^ sw) << 4);
+    st_shared_v4_b32(addr, pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                     pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+  }
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, buf, x0, y0);
+    bulk_commit_group();
+  }
 }
 
 template <int EPI, bool A_MN, bool B_MN, bool PAIR>
@@ -389,6 +409,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           cur = (ptr < K) ? __ldg(&args.pairs[rowK + ptr]) : make_int2(INT_MAX, 0);
         }
       }
+      if (EPI == kEpiDw && args.accumulate != 0 && row_ok) {
+        // The L2 add at the end of this unit reads the tile's current dW values:
+        // start bringing this row's part in from DRAM while the main loop runs.
+        const int c0 = d.n_begin * args.BN;
+        const int ncols = min(args.BN, args.Ncols - c0);
+        const float* src = args.out_f32 + static_cast<int64_t>(row) * args.ld_out + c0;
+        for (int c = 0; c < ncols; c += 32) prefetch_l2(src + c);
+      }
       for (int nb = d.n_begin; nb < d.n_end; ++nb) {
         const bool got = mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag, args.timeout_ns,
                                            args.status, 6);
@@ -404,7 +432,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int c = 0; c < kBNMax / 32; ++c) {
           if (32 * c >= args.BN) break;
           const int col0 = col_tile + 32 * c;
-          if (col0 >= args.Ncols && EPI != kEpiDz) break;
+          if (col0 >= args.Ncols) break;
           float v[32];
           __syncwarp();
           tmem_ld32(tacc + 32 * c, v);
@@ -452,16 +480,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) dv[i] = 0.0f;
             }
-            uint4* dst = reinterpret_cast<uint4*>(args.dz + static_cast<int64_t>(row) * args.dz_ld + col0);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              uint4 w;
-              w.x = pack_bf16x2(dv[8 * g + 0], dv[8 * g + 1]);
-              w.y = pack_bf16x2(dv[8 * g + 2], dv[8 * g + 3]);
-              w.z = pack_bf16x2(dv[8 * g + 4], dv[8 * g + 5]);
-              w.w = pack_bf16x2(dv[8 * g + 6], dv[8 * g + 7]);
-              dst[g] = w;
-            }
+            // Rows past the chunk's end are stored as zeros (the dW contraction
+            // reads them up to the next multiple of 64); columns past V are
+            // clipped by the TMA unit and never read back.
+            const int r0 = m0 + static_cast<int>(rank) * kBM + q * 32;
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            send_chunk_bf16(&tmC, my_staging + (sent & 1) * kOutChunkBytes, dv, lane, col0, r0);
+            ++sent;
           } else if (tma_out) {
             // dW, plain C, dH k-split partials: staged boxes, TMA store / add.
             // Boxes that start past the last row or column are not sent; the TMA

@@ -158,17 +158,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2D fp32 output map for the TMA store / add epilogue: `cols` contiguous
-// elements per row, `rows` rows, boxes of 16 x 32 with 64-byte swizzle.
-bool make_out_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes) {
+// 2D output map for the TMA store / add epilogue: `cols` contiguous elements
+// per row, `rows` rows, boxes of 32 rows x 64 bytes (16 fp32 or 32 bf16) with
+// 64-byte swizzle.
+bool make_out_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                  bool bf16 = false) {
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kOutBoxCols), 32};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(bf16 ? 32 : kOutBoxCols), 32};
   cuuint32_t es[2] = {1, 1};
   std::memset(m, 0, sizeof(*m));
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
-                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -431,8 +434,9 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
       !make_map(&mW_mn, W, D, V, rowH, 64, kBK) || !make_map(&mDz_mn, dz, V, L.C_pad, rowDz, 64, kBK) ||
       !make_map(&mH_mn, H, D, N, rowH, 64, kBK))
     return KD_ERR_CUDA;
-  CUtensorMap mDw_out, mDhp_out;
+  CUtensorMap mDw_out, mDhp_out, mDz_out;
   if (!make_out_map(&mDw_out, dW, D, V, static_cast<uint64_t>(D) * 4) ||
+      !make_out_map(&mDz_out, dz, V, L.C_pad, rowDz, true) ||
       (KS > 1 && !make_out_map(&mDhp_out, dhp, D, static_cast<uint64_t>(KS) * L.C_pad,
                                static_cast<uint64_t>(D) * 4)))
     return KD_ERR_CUDA;
@@ -465,7 +469,7 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     a.dz_ld = L.dz_ld;
     {
       ProfScope ps(kProfDzGemm, s);
-      if ((st = launch_gemm<kEpiDz, false, false, kPair>(mH_k, mW_k, mH_k, a, di, s)) != KD_OK)
+      if ((st = launch_gemm<kEpiDz, false, false, kPair>(mH_k, mW_k, mDz_out, a, di, s)) != KD_OK)
         return st;
     }
 
