@@ -125,16 +125,18 @@ __global__ void __launch_bounds__(kPrepWarps * 32)
     atomicAdd(n_valid, static_cast<unsigned long long>(s_count));
 }
 
-// One thread per row.
+// One thread per row. Rows of the forward's last row chunk were split over S_last
+// vocabulary ranges, all others over S_full.
 __global__ void __launch_bounds__(256)
-    kd_combine_kernel(Sched sc, int tile_rows, const float2* __restrict__ part, int slots,
+    kd_combine_kernel(int64_t last_start, int S_full, int S_last, const float2* __restrict__ part,
+                      int slots,
                       const int2* __restrict__ pairs, const float* __restrict__ zk,
                       const float* __restrict__ ent, const uint8_t* __restrict__ mask, int64_t N,
                       int K, int V, float inv_T, float* __restrict__ loss,
                       float* __restrict__ lse_out) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (row >= N) return;
-  const int S = sched_slots_for_block(sc, static_cast<int>(row / tile_rows));
+  const int S = row >= last_start ? S_last : S_full;  // vocabulary splits of the row's chunk
   float m = -INFINITY, s = 0.0f;
   for (int sl = 0; sl < S; ++sl) {
     const float2 ps = part[row * slots + sl];

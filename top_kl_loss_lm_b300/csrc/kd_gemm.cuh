@@ -73,7 +73,7 @@ struct GemmArgs {
   uint32_t idesc;
   int a_row_off;      // K-major A: row offset added to the tile row (chunk start in H)
   int b_k_off;        // MN-major B: k-row offset (chunk start in H for dW)
-  int64_t row_base;   // global token of local row 0 (dz, dh)
+  int64_t row_base;   // global token of local row 0 (fwd, dz, dh)
   int K;              // teacher top-K
   float scale2;       // log2(e) / T
   float inv_T;
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       float gs = 0.0f, lse2 = 0.0f;
       bool dz_row = false;
       if (EPI == kEpiFwd && row_ok) {
-        rowK = static_cast<int64_t>(row) * K;
+        rowK = (args.row_base + row) * K;
         ptr = lower_bound_id(args.pairs + rowK, K, d.n_begin * args.BN);
         cur.x = (ptr < K) ? __ldg(&args.pairs[rowK + ptr].x) : INT_MAX;
       }
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       if (EPI == kEpiFwd && ok && row_ok)
-        args.part[static_cast<int64_t>(row) * args.slots + d.slot] = make_float2(m2, s2);
+        args.part[(args.row_base + row) * args.slots + d.slot] = make_float2(m2, s2);
     }
     // The output boxes must be fully written before the kernel ends (and before
     // the staging memory is released).

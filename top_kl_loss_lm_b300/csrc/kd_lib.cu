@@ -280,6 +280,12 @@ kd_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   return cuda_check();
 }
 
+// Rows per forward launch: kPanelRows row blocks (one schedule panel).
+inline int64_t fwd_chunk_rows(int64_t N) {
+  const int64_t fc = static_cast<int64_t>(kPanelRows) * kTileRows;
+  return N < fc ? (N < 1 ? 1 : N) : fc;
+}
+
 // Persistent workers the GEMM schedules are planned for (CTA pairs).
 inline int gemm_slots(const DevInfo* di) { return kPair ? di->pair_slots : di->num_sms; }
 
@@ -360,11 +366,8 @@ extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const 
   if (!make_map(&mH, H, D, N, static_cast<uint64_t>(D) * 2, kBK, kBM) ||
       !make_map(&mW, W, D, V, static_cast<uint64_t>(D) * 2, kBK, Geo<kPair>::kBRows))
     return KD_ERR_CUDA;
-  const int MB = static_cast<int>(cdiv(N, kTileRows));
   const int KB = static_cast<int>(cdiv(D, kBK));
   GemmArgs a = base_args(di);
-  a.sched = make_panel_sched(MB, L.NB, KB, gemm_slots(di));
-  a.M = static_cast<int>(N);
   a.Ncols = V;
   a.BN = kBNMax;
   a.idesc = umma_idesc_bf16(kTileRows, kBNMax, false, false);
@@ -375,14 +378,27 @@ extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const 
   a.zk = zk;
   a.part = part;
   a.slots = L.slots;
-  {
+  // One launch per row chunk: the 74 CTA pairs then share the chunk's H rows
+  // and each W tile in L2, instead of spreading over rows from several panels.
+  const int64_t FC = fwd_chunk_rows(N);
+  int S_full = 0, S_last = 0;
+  const int64_t last_start = ((N - 1) / FC) * FC;
+  for (int64_t c0 = 0; c0 < N; c0 += FC) {
+    const int64_t rows = (N - c0) < FC ? (N - c0) : FC;
+    a.sched = make_panel_sched(static_cast<int>(cdiv(rows, kTileRows)), L.NB, KB, gemm_slots(di));
+    a.M = static_cast<int>(rows);
+    a.a_row_off = static_cast<int>(c0);
+    a.row_base = c0;
+    if (a.sched.P != 1) return KD_ERR_UNSUPPORTED;  // one panel per chunk by construction
+    if (c0 == 0) S_full = a.sched.S0;
+    if (c0 == last_start) S_last = a.sched.S0;
     ProfScope ps(kProfFwdGemm, s);
     if ((st = launch_gemm<kEpiFwd, false, false, kPair>(mH, mW, mH, a, di, s)) != KD_OK) return st;
   }
   {
     ProfScope ps(kProfCombine, s);
     kd_combine_kernel<<<static_cast<unsigned>(cdiv(N, 256)), 256, 0, s>>>(
-        a.sched, kTileRows, part, L.slots, pairs, zk, ent, mask, N, K, V, inv_T, loss, lse);
+        last_start, S_full, S_last, part, L.slots, pairs, zk, ent, mask, N, K, V, inv_T, loss, lse);
   }
   return cuda_check();
 }

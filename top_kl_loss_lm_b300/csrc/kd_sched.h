@@ -19,7 +19,7 @@ namespace kd {
 constexpr int kBM = 128;        // tile rows (MMA M)
 constexpr int kBK = 64;         // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kBNMax = 256;     // widest tile (MMA N)
-constexpr int kPanelRows = 32;  // row blocks per panel in the forward schedule
+constexpr int kPanelRows = 16;  // row blocks per panel (and per forward launch)
 constexpr int kMaxSlots = 64;   // max vocabulary splits per row (LSE partial slots)
 constexpr int kMaxKSplits = 8;  // max split of the dH contraction
 
@@ -69,12 +69,6 @@ KD_HD inline Unit sched_unit(const Sched& s, int64_t u) {
     d.slot = ks;
   }
   return d;
-}
-
-// Vocabulary splits used for the row block m_blk (panel mode).
-KD_HD inline int sched_slots_for_block(const Sched& s, int m_blk) {
-  const int p = m_blk / s.G0;
-  return (p >= s.P - 1) ? s.Sl : s.S0;
 }
 
 KD_HD inline int kd_gcd(int a, int b) {
