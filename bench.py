@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gptoss_32k")
     ap.add_argument("--chunk", type=int, default=4096)
+    ap.add_argument("--K", type=int, default=None, help="override the workload's teacher top-K")
+    ap.add_argument("--T", type=float, default=None, help="override the workload's temperature")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -261,7 +263,7 @@ def run_reference(args, rank, world):
     import torch
 
     from workloads import config_problem
-    p = config_problem(args.workload, seed=args.seed, device="cpu")
+    p = config_problem(args.workload, seed=args.seed, device="cpu", K=args.K, T=args.T)
     import numpy as np
 
     import oracle
@@ -352,7 +354,7 @@ def run_ours(args, rank, world, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    p = config_problem(args.workload, seed=args.seed + rank, device=dev)
+    p = config_problem(args.workload, seed=args.seed + rank, device=dev, K=args.K, T=args.T)
     head = Head(p, args.chunk)
     N, D, V = p.N, p.D, p.V
     flops_step = 8.0 * N * D * V

@@ -183,9 +183,17 @@ def test_gptoss_head_32k():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("K,T", [(8, 1.0), (64, 2.0), (256, 1.0)])
+@pytest.mark.parametrize("K", [8, 64, 256])
+@pytest.mark.parametrize("T", [1.0, 2.0])
 def test_packed_documents(K, T):
     _check_sampled(config_problem("packed_qwen", device=DEV, K=K, T=T))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("N", [131072, 262144])
+def test_gptoss_head_long_sweep(N):
+    # the largest sizes of the memory / rate sweep, sampled rows + row-sum property
+    _check_sampled(config_problem("gptoss_32k", device=DEV, N=N))
 
 
 @pytest.mark.slow
