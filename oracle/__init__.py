@@ -3,6 +3,7 @@ from .kd_oracle import (  # noqa: F401
     dense_teacher_grid,
     kd_backward,
     kd_forward,
+    kd_from_logits,
     logsumexp_rows,
     mean_loss,
     student_logits,

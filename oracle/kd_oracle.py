@@ -46,6 +46,7 @@ __all__ = [
     "kd_backward",
     "mean_loss",
     "dense_teacher_grid",
+    "kd_from_logits",
 ]
 
 
@@ -162,3 +163,42 @@ def kd_backward(H, W, idx, t, mask, T: float, g, row_chunk: int = 64):
         dH[rows] = dZ @ W
         dW += dZ.T @ H[rows]
     return dH, dW
+
+
+def kd_from_logits(Z, idx, t, mask, T: float, g=None, row_chunk: int = 64):
+    """The same loss and its logit gradient, from logits that were already computed.
+
+    The forward-chunked bullet (blog "Two systems changes") keeps the teacher
+    sparse and computes the loss one slice of positions at a time from the
+    student's logits, which the output layer has produced in full beforehand.
+    Per row n of Z (fp64):
+      a = Z[n]/T,  lse_n = logsumexp(a),  loss_n = sum_{P_j > 0} P_j (log P_j - (a_j - lse_n))
+      dZ[n, j] = (g_n/T) (exp(a_j - lse_n) - p~[n, j])   (0 on masked rows)
+    with P / p~ the dense teacher grid of the row, exactly as in kd_forward and
+    kd_backward. Returns (loss[N], lse[N], n_valid, dZ[N, V] or None when g is None).
+    """
+    Z = np.asarray(Z, dtype=np.float64)
+    idx = np.asarray(idx)
+    t = np.asarray(t)
+    mask = np.asarray(mask).astype(bool)
+    N, V = Z.shape
+    loss = np.zeros(N, dtype=np.float64)
+    lse = np.zeros(N, dtype=np.float64)
+    dZ = None if g is None else np.zeros((N, V), dtype=np.float64)
+    for r0, r1 in _blocks(N, row_chunk):
+        a = Z[r0:r1] / T
+        lse[r0:r1] = logsumexp_rows(a)
+        valid = np.nonzero(mask[r0:r1])[0]
+        if valid.size == 0:
+            continue
+        logp = teacher_log_probs(t[r0:r1][valid], T)
+        P = dense_teacher_grid(idx[r0:r1][valid].astype(np.int64), logp, V)
+        log_q = a[valid] - lse[r0:r1][valid][:, None]
+        pos = P > 0
+        terms = np.zeros_like(P)
+        terms[pos] = P[pos] * (np.log(P[pos]) - log_q[pos])
+        loss[r0 + valid] = np.sum(terms, axis=1)
+        if dZ is not None:
+            gv = np.asarray(g, dtype=np.float64)[r0 + valid]
+            dZ[r0 + valid] = (gv / T)[:, None] * (np.exp(log_q) - P)
+    return loss, lse, int(mask.sum()), dZ

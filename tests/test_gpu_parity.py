@@ -42,6 +42,14 @@ def test_several_tiles_and_chunks():
     _full(p, chunk=384)
 
 
+def test_forward_row_chunks_with_ragged_tail():
+    # the forward is launched per 4,096 rows: two full chunks and a ragged third one,
+    # with the backward's chunks (1,536 rows) cutting across the forward's
+    p = make_problem(2 * 4096 + 300, 72, 1800, 16, 1.2, seed=15, mask="frac", mask_frac=0.03,
+                     garbage_masked=True, device=DEV)
+    _full(p, chunk=1536)
+
+
 @pytest.mark.parametrize("T", [0.7, 2.0])
 def test_teacher_covers_vocabulary(T):
     p = make_problem(64, 64, 200, 200, T, seed=3, device=DEV)

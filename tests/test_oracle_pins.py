@@ -302,3 +302,72 @@ def test_dense_grid_bytes_match_pages_example():
     b = dense_grid_bytes(int(fx["batch"]) * int(fx["seq"]), int(fx["vocab"]), int(fx["bytes_per_elem"]))
     assert b == 4 * 201088 * 32768 * 2
     assert abs(b / 1e9 - fx["approx_gb"]) / fx["approx_gb"] < 0.1
+
+
+# ----------------------------------------------------------------------------- logits-input form
+
+
+def _library_dense_kl_logits(Z, idx, t, mask, T, g):
+    """torch kl_div of the dense teacher grid against log_softmax(Z/T), autograd wrt Z."""
+    Zt = torch.tensor(Z, dtype=torch.float64, requires_grad=True)
+    N, V = Z.shape
+    P = torch.zeros(N, V, dtype=torch.float64)
+    for n in range(N):
+        if not mask[n]:
+            continue
+        pk = torch.softmax(torch.tensor(t[n], dtype=torch.float64) / T, dim=0)
+        for k in range(idx.shape[1]):
+            P[n, int(idx[n, k])] += pk[k]
+    kl = torch.nn.functional.kl_div(torch.log_softmax(Zt / T, dim=1), P, reduction="none").sum(dim=1)
+    kl = torch.where(torch.tensor(mask.astype(bool)), kl, torch.zeros_like(kl))
+    (kl * torch.tensor(g, dtype=torch.float64)).sum().backward()
+    return kl.detach().numpy(), Zt.grad.numpy()
+
+
+@pytest.mark.parametrize("T", [0.6, 1.5])
+def test_logits_form_matches_library(T):
+    H, W, idx, t, mask = _rand_problem(21, 7, 5, 17, 4, masked=(3,), dup_row=5)
+    Z = H @ W.T * 2.0
+    g = np.linspace(-1.0, 2.0, 7)
+    loss, lse, nv, dZ = oracle.kd_from_logits(Z, idx, t, mask, T, g, row_chunk=3)
+    lib, ldZ = _library_dense_kl_logits(Z, idx, t, mask, T, g)
+    assert _rel(loss, lib) < 1e-12
+    assert _rel(lse, torch.logsumexp(torch.tensor(Z) / T, dim=1).numpy()) < 1e-13
+    assert _rel(dZ, ldZ) < 1e-12
+    assert nv == 6
+
+
+def test_logits_form_chains_to_head_gradients():
+    # with Z = H W^T the logit gradient must give the head oracle's dH = dZ W and dW = dZ^T H
+    H, W, idx, t, mask = _rand_problem(22, 9, 6, 23, 5, masked=(0, 4), dup_row=2)
+    g = np.linspace(0.1, 1.0, 9)
+    for T in (1.0, 1.8):
+        loss, lse, nv, dZ = oracle.kd_from_logits(H @ W.T, idx, t, mask, T, g)
+        l2, lse2, nv2 = oracle.kd_forward(H, W, idx, t, mask, T)
+        dH, dW = oracle.kd_backward(H, W, idx, t, mask, T, g)
+        assert _rel(loss, l2) < 1e-13 and _rel(lse, lse2) < 1e-13 and nv == nv2
+        assert _rel(dZ @ W, dH) < 1e-12 and _rel(dZ.T @ H, dW) < 1e-12
+        assert np.all(dZ[mask == 0] == 0)
+
+
+def test_logits_form_finite_differences():
+    rng = np.random.default_rng(23)
+    Z = rng.standard_normal((3, 8)) * 2.0
+    idx = np.array([[1, 5, 5], [0, 2, 7], [3, 4, 6]])  # row 0 repeats an id
+    t = np.sort(rng.standard_normal((3, 3)), axis=1)[:, ::-1].copy()
+    mask = np.array([1, 0, 1], dtype=np.uint8)
+    g = np.array([0.9, 1.1, -0.6])
+    for T in (1.0, 0.7):
+        _, _, _, dZ = oracle.kd_from_logits(Z, idx, t, mask, T, g)
+
+        def f(Zx):
+            return float(np.dot(g, oracle.kd_from_logits(Zx, idx, t, mask, T)[0]))
+
+        h = 1e-6
+        num = np.zeros_like(Z)
+        for i in range(Z.shape[0]):
+            for j in range(Z.shape[1]):
+                Zp = Z.copy(); Zp[i, j] += h
+                Zm = Z.copy(); Zm[i, j] -= h
+                num[i, j] = (f(Zp) - f(Zm)) / (2 * h)
+        assert _rel(dZ, num) < 1e-7
