@@ -56,7 +56,7 @@ def parse():
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_gptoss_32k.json")
-KERNEL_SOURCES = ("kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h")
+KERNEL_SOURCES = ("kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h", "kd_logits.cuh")
 # template argument of kd_gemm_kernel -> category of the library's launch timing
 GEMM_EPI = {"0": "fwd_gemm", "1": "dz_gemm", "2": "dh_gemm", "3": "dw_gemm"}
 

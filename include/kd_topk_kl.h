@@ -103,6 +103,36 @@ kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const int32_t* to
                          void* ws, size_t ws_bytes, kd_stream_t stream);
 
 /*
+ * The loss from logits the caller has already computed, and optionally its
+ * gradient with respect to those logits: the forward-chunked form (blog "Making
+ * Knowledge Distillation Cheap Enough to Run at Scale", section "Two systems
+ * changes", forward-chunked KL bullet: the teacher stays sparse and the loss is
+ * computed one slice of sequence positions at a time, from student logits the
+ * output layer produced beforehand). Call it once per slice of rows to bound
+ * memory; rows are independent.
+ *   Z      [N x V] bf16 logits, row stride ldz elements (ldz >= V).
+ *   dloss  [N] fp32 upstream gradient (1/n_valid at counted rows for the mean
+ *          loss), or NULL to compute the loss only.
+ *   dZ     [N x V] bf16 output dZ = (dloss/T)(softmax(Z/T) - P), 0 at masked
+ *          rows; row stride lddz; or NULL. It may be Z itself: the gradient
+ *          then overwrites the logits (each row is read completely before its
+ *          gradient is written).
+ *   loss, lse, n_valid, topk_idx, topk_logit, mask, T: as in kd_topk_kl_fwd
+ *          (lse = logsumexp(Z/T) for every row).
+ *   ws     at least kd_topk_kl_logits_workspace_size(N, K) bytes.
+ * V, ldz and lddz must be multiples of 8 (16-byte row starts; KD_ERR_ALIGN
+ * otherwise); V up to about 460,000 (KD_ERR_UNSUPPORTED beyond). Z, dZ 16-byte
+ * aligned, ws 256-byte aligned. dZ given without dloss is KD_ERR_ARG.
+ */
+size_t kd_topk_kl_logits_workspace_size(int64_t N, int K);
+
+kd_status kd_topk_kl_logits(const uint16_t* Z, int64_t ldz, const int32_t* topk_idx,
+                            const float* topk_logit, const uint8_t* mask, const float* dloss,
+                            int64_t N, int V, int K, float T, float* loss, float* lse,
+                            int64_t* n_valid, uint16_t* dZ, int64_t lddz, void* ws,
+                            size_t ws_bytes, kd_stream_t stream);
+
+/*
  * Forward with no workspace argument and no allocation, for callers that
  * cannot obtain device memory themselves (a plugin inside a process whose own
  * allocator already holds the GPU's memory, or a hot path where cudaMalloc,

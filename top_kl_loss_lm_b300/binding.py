@@ -18,6 +18,7 @@ import torch
 __all__ = [
     "KdError", "lib", "library_path",
     "kd_topk_kl_workspace_size", "kd_topk_kl_fwd", "kd_topk_kl_bwd", "kd_topk_kl_fwd_noalloc",
+    "kd_topk_kl_logits_workspace_size", "kd_topk_kl_logits",
     "kd_get_status", "kd_status_string",
     "kd_debug_gemm_bf16", "kd_debug_wait_timeout", "kd_debug_schedule",
     "kd_debug_profile", "kd_debug_profile_read", "PROFILE_CATEGORIES",
@@ -65,6 +66,11 @@ def lib() -> ctypes.CDLL:
         L.kd_topk_kl_bwd.restype = i32
         L.kd_topk_kl_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp, vp]
         L.kd_topk_kl_fwd_noalloc.restype = i32
+        L.kd_topk_kl_logits_workspace_size.argtypes = [i64, i32]
+        L.kd_topk_kl_logits_workspace_size.restype = sz
+        L.kd_topk_kl_logits.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, f32, vp, vp, vp, vp,
+                                        i64, vp, sz, vp]
+        L.kd_topk_kl_logits.restype = i32
         L.kd_get_status.argtypes = [vp]
         L.kd_get_status.restype = i32
         L.kd_status_string.argtypes = [i32]
@@ -180,6 +186,42 @@ def kd_topk_kl_bwd(H, W, topk_idx, topk_logit, mask, lse, dloss, T: float, chunk
     _check(lib().kd_topk_kl_bwd(*args), "kd_topk_kl_bwd")
 
 
+def kd_topk_kl_logits_workspace_size(N: int, K: int) -> int:
+    return int(lib().kd_topk_kl_logits_workspace_size(N, K))
+
+
+def _rows_ptr(t: torch.Tensor, name: str, N: int, V: int, device):
+    """Data pointer and row stride of an N x V bf16 matrix whose rows are contiguous."""
+    if t.dtype != torch.bfloat16 or tuple(t.shape) != (N, V):
+        raise ValueError(f"{name}: expected bfloat16 of shape {(N, V)}, got {t.dtype} {tuple(t.shape)}")
+    if t.stride(1) != 1 or (N > 1 and t.stride(0) < V):
+        raise ValueError(f"{name}: rows must be contiguous")
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name}: must be on {device}")
+    return t.data_ptr(), (t.stride(0) if N > 1 else V)
+
+
+def kd_topk_kl_logits(Z, topk_idx, topk_logit, mask, T: float, loss, lse, n_valid, ws,
+                      dloss=None, dZ=None, stream=None):
+    """Loss (and dZ when dloss and dZ are given) from materialised bf16 logits Z [N x V]."""
+    N, V = Z.shape
+    K = topk_idx.shape[1]
+    dev = Z.device
+    zp, ldz = _rows_ptr(Z, "Z", N, V, dev)
+    dp, lddz = (None, 0) if dZ is None else _rows_ptr(dZ, "dZ", N, V, dev)
+    args = (
+        zp, ldz, _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
+        _ptr(topk_logit, torch.float32, (N, K), "topk_logit", dev),
+        _ptr(mask, torch.uint8, (N,), "mask", dev),
+        _ptr(dloss, torch.float32, (N,), "dloss", dev),
+        N, V, K, float(T),
+        _ptr(loss, torch.float32, (N,), "loss", dev), _ptr(lse, torch.float32, (N,), "lse", dev),
+        _ptr(n_valid, torch.int64, (1,), "n_valid", dev), dp, lddz,
+        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream),
+    )
+    _check(lib().kd_topk_kl_logits(*args), "kd_topk_kl_logits")
+
+
 def kd_get_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
     return int(lib().kd_get_status(_stream(stream)))
@@ -225,7 +267,8 @@ def kd_debug_schedule(kind: int, rows: int, cols: int, depth: int, grid_units: i
     return {k: int(v) for k, v in zip(keys, info)}, counts
 
 
-PROFILE_CATEGORIES = ["prep", "fwd_gemm", "combine", "dz_gemm", "dh_gemm", "dh_sum", "dw_gemm"]
+PROFILE_CATEGORIES = ["prep", "fwd_gemm", "combine", "dz_gemm", "dh_gemm", "dh_sum", "dw_gemm",
+                      "logits"]
 
 
 def kd_debug_profile(enable: bool):

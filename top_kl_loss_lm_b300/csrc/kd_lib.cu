@@ -21,6 +21,7 @@
 #include "../../include/kd_topk_kl_testing.h"
 #include "kd_aux.cuh"
 #include "kd_gemm.cuh"
+#include "kd_logits.cuh"
 #include "kd_sched.h"
 
 namespace kd {
@@ -50,7 +51,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // Optional per-launch timing (test hook kd_debug_profile): a start/stop event
 // pair recorded on the launching stream around every kernel of the library.
 enum ProfCat : int { kProfPrep = 0, kProfFwdGemm, kProfCombine, kProfDzGemm, kProfDhGemm, kProfDhSum,
-                     kProfDwGemm, kProfCats };
+                     kProfDwGemm, kProfLogits, kProfCats };
 struct Prof {
   bool on = false;
   std::vector<cudaEvent_t> ev;      // pool: 2 per record
@@ -534,6 +535,138 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     }
   }
   return KD_OK;
+}
+
+// ------------------------------------------------------------------ loss from materialised logits
+
+namespace kd {
+namespace {
+
+// Columns per CTA slice for a cluster of `cl` CTAs: a multiple of 64 so each slice
+// starts on a 128-byte line.
+inline int logits_slice(int V, int cl) { return static_cast<int>(cdiv(cdiv(V, cl), 64) * 64); }
+
+constexpr size_t kLogitsSmemLimit = 227 * 1024;
+
+// Smallest cluster whose slices (two row buffers each) fit in shared memory.
+int logits_cluster(int V) {
+  for (int cl = 1; cl <= kLogitsMaxCluster; cl *= 2)
+    if (logits_smem_bytes(logits_slice(V, cl)) <= kLogitsSmemLimit) return cl;
+  return 0;
+}
+
+template <int CL>
+kd_status launch_logits(const LogitsArgs& a, const DevInfo* di, cudaStream_t s) {
+  auto kern = kd_logits_kernel<CL>;
+  const size_t smem = logits_smem_bytes(a.Vs);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess) {
+    cudaGetLastError();
+    return KD_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(di->num_sms / CL * CL));
+  cfg.blockDim = dim3(kLogitsThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+    cudaGetLastError();
+    clusters = di->num_sms / CL;
+  }
+  int64_t want = a.N < clusters ? a.N : clusters;
+  if (want < 1) return KD_OK;
+  cfg.gridDim = dim3(static_cast<unsigned>(want * CL));
+  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) {
+    cudaGetLastError();
+    return KD_ERR_CUDA;
+  }
+  return cuda_check();
+}
+
+}  // namespace
+}  // namespace kd
+
+extern "C" size_t kd_topk_kl_logits_workspace_size(int64_t N, int K) {
+  if (N < 0 || K < 1 || K > kMaxTopK) return 0;
+  const size_t pairs = align256(static_cast<size_t>(N) * K * sizeof(int2));
+  const size_t ent = align256(static_cast<size_t>(N) * sizeof(float));
+  const size_t total = pairs + ent;
+  return total > 0 ? total : 256;
+}
+
+extern "C" kd_status kd_topk_kl_logits(const uint16_t* Z, int64_t ldz, const int32_t* topk_idx,
+                                       const float* topk_logit, const uint8_t* mask,
+                                       const float* dloss, int64_t N, int V, int K, float T,
+                                       float* loss, float* lse, int64_t* n_valid, uint16_t* dZ,
+                                       int64_t lddz, void* ws, size_t ws_bytes,
+                                       kd_stream_t stream) {
+  if (N < 0 || V <= 0 || K < 1 || K > kMaxTopK || !(T > 0.0f) || !std::isfinite(T))
+    return KD_ERR_ARG;
+  if (N > (int64_t(1) << 40) || V > (1 << 30)) return KD_ERR_UNSUPPORTED;
+  if (!n_valid) return KD_ERR_ARG;
+  if (N > 0 && (!Z || !topk_idx || !topk_logit || !loss || !lse || !ws)) return KD_ERR_ARG;
+  if (dZ && !dloss) return KD_ERR_ARG;
+  if (ldz < V || (dZ && lddz < V)) return KD_ERR_ARG;
+  if (V % 8 != 0 || ldz % 8 != 0 || (dZ && lddz % 8 != 0)) return KD_ERR_ALIGN;
+  if (!aligned(Z, 16) || (dZ && !aligned(dZ, 16)) || !aligned(ws, 256) || !aligned(topk_idx, 4) ||
+      !aligned(topk_logit, 4) || !aligned(loss, 4) || !aligned(lse, 4) || !aligned(n_valid, 8) ||
+      (dloss && !aligned(dloss, 4)))
+    return KD_ERR_ALIGN;
+  const int cl = logits_cluster(V);
+  if (cl == 0) return KD_ERR_UNSUPPORTED;
+  kd_status st = KD_OK;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s) != cudaSuccess) return KD_ERR_CUDA;
+  if (N == 0) return KD_OK;
+  if (ws_bytes < kd_topk_kl_logits_workspace_size(N, K)) return KD_ERR_WORKSPACE;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int2* pairs = reinterpret_cast<int2*>(w);
+  float* ent = reinterpret_cast<float*>(w + align256(static_cast<size_t>(N) * K * sizeof(int2)));
+  const float inv_T = 1.0f / T;
+  {
+    ProfScope ps(kProfPrep, s);
+    kd_prep_kernel<<<static_cast<unsigned>(cdiv(N, kPrepWarps)), kPrepWarps * 32, 0, s>>>(
+        topk_idx, topk_logit, mask, N, K, V, inv_T, pairs, ent,
+        reinterpret_cast<unsigned long long*>(n_valid), di->status);
+  }
+  if ((st = cuda_check()) != KD_OK) return st;
+  LogitsArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.Z = Z;
+  a.ldz = ldz;
+  a.dZ = dZ;
+  a.lddz = lddz;
+  a.pairs = pairs;
+  a.ent = ent;
+  a.mask = mask;
+  a.dloss = dloss;
+  a.loss = loss;
+  a.lse = lse;
+  a.N = N;
+  a.V = V;
+  a.K = K;
+  a.Vs = logits_slice(V, cl);
+  a.scale2 = 1.4426950408889634f * inv_T;
+  a.inv_T = inv_T;
+  a.status = di->status;
+  a.timeout_ns = 2000000000ull;
+  ProfScope ps(kProfLogits, s);
+  switch (cl) {
+    case 1: return launch_logits<1>(a, di, s);
+    case 2: return launch_logits<2>(a, di, s);
+    case 4: return launch_logits<4>(a, di, s);
+    default: return launch_logits<8>(a, di, s);
+  }
 }
 
 extern "C" kd_status kd_get_status(kd_stream_t stream) {
