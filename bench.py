@@ -50,12 +50,16 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--logits", action="store_true",
+                    help="measure the loss from materialised logits (kd_topk_kl_logits) instead")
+    ap.add_argument("--logits-rows", type=int, default=32768)
     ap.add_argument("--traffic-from", default=None,
                     help="write the per-launch DRAM traffic record from this ncu --csv log and exit")
     return ap.parse_args()
 
 
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_gptoss_32k.json")
+def traffic_file(workload: str) -> str:
+    return os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.json")
 KERNEL_SOURCES = ("kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h", "kd_logits.cuh")
 # template argument of kd_gemm_kernel -> category of the library's launch timing
 GEMM_EPI = {"0": "fwd_gemm", "1": "dz_gemm", "2": "dh_gemm", "3": "dw_gemm"}
@@ -86,13 +90,15 @@ def traffic_from_ncu_csv(csv_path: str, workload: str, chunk: int) -> dict:
                 continue
             d = dict(zip(hdr, r))
             m = re.search(r"kd_gemm_kernel<(\d)", d["Kernel Name"])
-            if not m or d["Metric Name"] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            cat = GEMM_EPI[m.group(1)] if m else ("logits" if "kd_logits_kernel" in d["Kernel Name"]
+                                                  else None)
+            if cat is None or d["Metric Name"] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
                 continue
             unit = d.get("Metric Unit", "byte").lower()
             scale = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9}.get(unit, 1)
             v = float(d["Metric Value"].replace(",", "")) * scale
-            per.setdefault(GEMM_EPI[m.group(1)], {}).setdefault(d["ID"], 0.0)
-            per[GEMM_EPI[m.group(1)]][d["ID"]] += v
+            per.setdefault(cat, {}).setdefault(d["ID"], 0.0)
+            per[cat][d["ID"]] += v
     return {"source_hash": kernel_source_hash(), "workload": workload, "chunk_tokens": chunk,
             "bytes_per_launch": {k: sum(v.values()) / len(v) for k, v in per.items()},
             "launches": {k: len(v) for k, v in per.items()}}
@@ -102,7 +108,7 @@ def recorded_traffic(kernel: str, workload: str, chunk: int):
     """DRAM bytes per launch recorded for this kernel, or None when the record is
     missing, for another workload, or taken from different kernel sources."""
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(traffic_file(workload)) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
@@ -497,6 +503,122 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+LOGITS_METRIC = "top-K KL + logit gradient from materialised logits: tokens/s; HBM GB/s"
+
+
+def run_logits(args):
+    """The forward-chunked form: loss and dZ from bf16 logits already in HBM.
+
+    One step = one kd_topk_kl_logits call over N rows of V logits (the
+    gpt-oss head's vocabulary) with the gradient written to a separate buffer.
+    """
+    import torch
+
+    from top_kl_loss_lm_b300 import binding
+    from workloads import make_problem, mean_upstream_grad
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    N, V = args.logits_rows, 201088
+    K = args.K or 64
+    T = args.T or 1.0
+    p = make_problem(N, 8, V, K, T, seed=args.seed, mask="frac", mask_frac=0.02, device=dev,
+                     name="gptoss_logits")
+    g = torch.Generator(device=dev).manual_seed(args.seed + 7)
+    Z = torch.empty(N, V, dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, N, 4096):
+        r1 = min(N, r0 + 4096)
+        Z[r0:r1] = (3.0 * torch.randn(r1 - r0, V, device=dev, generator=g)).to(torch.bfloat16)
+    dZ = torch.empty_like(Z)
+    ws = torch.empty(binding.kd_topk_kl_logits_workspace_size(N, K), dtype=torch.uint8, device=dev)
+    loss = torch.empty(N, device=dev)
+    lse = torch.empty(N, device=dev)
+    nv = torch.empty(1, dtype=torch.int64, device=dev)
+    dl = mean_upstream_grad(p.mask).to(dev)
+
+    def step():
+        binding.kd_topk_kl_logits(Z, p.idx, p.t, p.mask, T, loss, lse, nv, ws, dloss=dl, dZ=dZ)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if binding.kd_get_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    sampler = ClockSampler(0)
+    torch.cuda.synchronize()
+    sampler.start()
+    binding.kd_debug_profile(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    prof = binding.kd_debug_profile_read()
+    binding.kd_debug_profile(False)
+    if binding.kd_get_status() != 0:
+        raise RuntimeError("device status in the timed region")
+    ms = e0.elapsed_time(e1)
+    tot, n = prof["logits"]
+    # algorithmic bytes of one launch: logits read once, dZ written once, the sorted
+    # teacher pairs read, and per row: mask, dloss, entropy read, loss and lse written
+    per_launch = N * V * 2 * 2 + N * K * 8 + N * (1 + 4 + 4 + 4 + 4)
+    achieved = per_launch / (tot / n / 1000.0) / 1e9
+    peaks, src = load_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    cpu = None
+    if not args.no_cpu_baseline:
+        import numpy as np
+
+        import oracle
+        rng = np.random.default_rng(args.seed)
+        idx, t, m = p.idx.cpu().numpy(), p.t.double().cpu().numpy(), p.mask.cpu().numpy()
+        done, secs = 0, 0.0
+        while secs < args.cpu_seconds and done < 4096:
+            rows = np.sort(rng.choice(N, size=64, replace=False))
+            Zs = Z[torch.as_tensor(rows, device=dev)].double().cpu().numpy()
+            t0 = time.perf_counter()
+            oracle.kd_from_logits(Zs, idx[rows], t[rows], m[rows], T, m[rows] / max(int(m.sum()), 1))
+            secs += time.perf_counter() - t0
+            done += len(rows)
+        try:
+            from threadpoolctl import threadpool_info
+            threads = max(int(d.get("num_threads", 1)) for d in threadpool_info())
+        except Exception:
+            threads = os.cpu_count()
+        cpu = {"value": done / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{done} seeded rows of {N} in 64-row calls ({secs:.1f} s); the oracle is "
+                         f"row-additive, so rows/s is its tokens/s"}
+    line = {
+        "metric": LOGITS_METRIC, "value": args.steps * N / (ms / 1000.0), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"gptoss_logits: N={N} rows of V={V} bf16 logits, K={K}, T={T}",
+                   "N": N, "V": V, "K": K, "T": T, "masked_rows": int(N - int(p.mask.sum().item())),
+                   "l2": "inputs larger than L2 (the logits are %.1f GB)" % (N * V * 2 / 1e9),
+                   "inputs": "logits 3*N(0,1) in bf16; teacher ids distinct uniform, logits "
+                             "N(0,4)+Gumbel sorted"},
+        "roofline": {"bound": "hbm", "kernel": "kd_logits_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": recorded_traffic("logits", "gptoss_logits", 0),
+                     "traffic_unit": "bytes per launch (dram read + write, ncu)",
+                     "peak_kind": f"HBM copy bandwidth ({src})",
+                     "bytes_per_launch": per_launch},
+        "kernels": {c: {"ms_per_step": prof[c][0] / args.steps,
+                        "launches_per_step": prof[c][1] / args.steps}
+                    for c in prof if prof[c][1]},
+        "gpu_launches": int(sum(c[1] for c in prof.values())),
+        "clocks": clocks, "e2e": None, "cpu_baseline": cpu,
+        "note": "secondary line (the next row after the fused head); e2e omitted: the logits "
+                "would be copied from host memory every step",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_sweep(args):
     """Peak device memory and rate vs N (D, V, K of the gpt-oss head)."""
     import torch
@@ -532,8 +654,9 @@ def run_sweep(args):
 def main():
     args = parse()
     if args.traffic_from:
-        rec = traffic_from_ncu_csv(args.traffic_from, args.workload, args.chunk)
-        with open(TRAFFIC_FILE, "w") as f:
+        name, chunk = ("gptoss_logits", 0) if args.logits else (args.workload, args.chunk)
+        rec = traffic_from_ncu_csv(args.traffic_from, name, chunk)
+        with open(traffic_file(name), "w") as f:
             json.dump(rec, f, indent=1)
         print(json.dumps(rec))
         return 0
@@ -542,6 +665,8 @@ def main():
         return run_reference(args, rank, world)
     if args.sweep:
         return run_sweep(args)
+    if args.logits:
+        return run_logits(args)
     return run_ours(args, rank, world, local)
 
 

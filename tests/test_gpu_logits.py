@@ -1,11 +1,11 @@
 """Parity of kd_topk_kl_logits (loss and logit gradient from materialised logits)
 with the CPU fp64 oracle's kd_from_logits, through the C ABI.
 
-Small cases compare every element; the cluster sizes 1, 2, 4 and 8 (one row
-split over that many CTAs) are each exercised by a vocabulary size that needs
-them; the full-size case (N = 32,768 rows of the 201,088-token head) is
-checked on sampled rows plus the property that every counted row of dZ sums to
-zero.
+Small cases compare every element; every cluster size (one row split over 1,
+2, 4 or 8 CTAs), with one or two CTAs per SM, is exercised by a vocabulary
+size that needs it; the full-size case (N = 32,768
+rows of the 201,088-token head) is checked on sampled rows plus the property
+that every counted row of dZ sums to zero.
 """
 import numpy as np
 import pytest
@@ -67,10 +67,14 @@ def test_small_every_element():
     _compare(p, Z, _run(p, Z))
 
 
-@pytest.mark.parametrize("V,cluster", [(4096, 1), (100000, 2), (201088, 4), (300000, 8)])
-def test_cluster_sizes(V, cluster):
-    # one row is split over `cluster` CTAs whose slices meet through distributed shared memory
-    p, Z = _logits_problem(40, V, 64, 1.0, seed=2 + cluster, mask="frac", mask_frac=0.05)
+# (V, cluster size x CTAs per SM the library picks for it, rows: ~8+ per cluster)
+@pytest.mark.parametrize("V,shape,N", [(4096, "1x2", 2400), (40000, "2x2", 1200),
+                                       (100000, "4x2", 600), (201088, "8x2", 300),
+                                       (300000, "8x1", 200), (400000, "8x1", 150)])
+def test_cluster_sizes(V, shape, N):
+    # one row is split over a cluster of CTAs whose slices meet through distributed
+    # shared memory; more rows than clusters, so every ring buffer is reused
+    p, Z = _logits_problem(N, V, 64, 1.0, seed=V % 97, mask="frac", mask_frac=0.05)
     _compare(p, Z, _run(p, Z))
 
 

@@ -17,9 +17,14 @@
 //            bf16 in place; the teacher's ids get their exact fp32 value
 //            (repeated ids merged) before rounding; then one bulk store
 //
-// Two row buffers per CTA: the next row's bulk copy runs while this row is
-// reduced. Every wait is bounded; a CTA that gives up keeps taking part in the
-// cluster barriers (so no peer can wait forever) and only skips work.
+// Warp 0 is the copy engine's driver: it keeps NBUF row buffers in a ring (the
+// library uses two), loading the next row while this one is reduced and
+// storing each finished dZ row; warps 1..8 compute. Two such CTAs share an SM
+// when the slices are small enough, so each SM runs two row pipelines. Partials travel to every CTA of the cluster with st.async onto an
+// mbarrier, so no cluster-wide barrier sits in the row loop and the copies
+// never wait on the arithmetic. Every wait is bounded: a CTA that gives up
+// records KD_ERR_TIMEOUT, skips the remaining work, and its peers' waits for
+// its partials run out in turn.
 #pragma once
 
 #include <climits>
@@ -30,9 +35,11 @@
 
 namespace kd {
 
-constexpr int kLogitsThreads = 256;
+constexpr int kLogitsThreads = 256;  // compute threads (warps 1..8); warp 0 drives the copies
 constexpr int kLogitsWarps = kLogitsThreads / 32;
+constexpr int kLogitsBlock = kLogitsThreads + 32;
 constexpr int kLogitsMaxCluster = 8;
+constexpr int kLogitsMaxBuffers = 4;
 
 struct LogitsArgs {
   const uint16_t* Z;     // N x V bf16 logits, row stride ldz elements
@@ -53,11 +60,12 @@ struct LogitsArgs {
   uint64_t timeout_ns;
 };
 
-__host__ __device__ constexpr size_t logits_smem_bytes(int Vs) {
-  return 2 * static_cast<size_t>(Vs) * 2       // two row buffers (bf16)
-         + 2 * kLogitsMaxCluster * 16           // cluster exchange slots, two parities
-         + kLogitsWarps * 16                    // block reduction scratch
-         + 2 * 8 + 16;                          // two mbarriers, abort flag
+// Shared memory of one CTA: NBUF row slices, then the small parts.
+__host__ __device__ constexpr size_t logits_smem_bytes(int Vs, int nbuf) {
+  return static_cast<size_t>(nbuf) * Vs * 2      // row slices (bf16)
+         + 2 * kLogitsMaxCluster * 16            // cluster partials, two parities
+         + 2 * kLogitsWarps * 16                 // block reduction scratch, two parities
+         + (2 * kLogitsMaxBuffers + 2) * 8 + 16; // full / empty / exchange barriers, abort flag
 }
 
 __device__ __forceinline__ float2 merge_ms(float2 a, float2 b) {
@@ -74,176 +82,215 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int CL>
-__global__ void __launch_bounds__(kLogitsThreads, 1) kd_logits_kernel(const LogitsArgs a) {
+// Barrier among the compute warps only (named barrier 1).
+__device__ __forceinline__ void compute_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kLogitsThreads) : "memory");
+}
+
+template <int CL, int NBUF>
+__global__ void __launch_bounds__(kLogitsBlock, 2) kd_logits_kernel(const LogitsArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  auto buf = [&](int b) { return reinterpret_cast<uint16_t*>(smem + static_cast<size_t>(b) * a.Vs * 2); };
-  float4* exch = reinterpret_cast<float4*>(smem + static_cast<size_t>(a.Vs) * 4);  // [2][CL]
-  float4* red = exch + 2 * kLogitsMaxCluster;                                     // [warps]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + kLogitsWarps);               // [2]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+  const size_t slice_bytes = static_cast<size_t>(a.Vs) * 2;
+  auto buf = [&](int b) { return reinterpret_cast<uint16_t*>(smem + b * slice_bytes); };
+  float4* exch = reinterpret_cast<float4*>(smem + NBUF * slice_bytes);  // [2][kLogitsMaxCluster]
+  float4* red = exch + 2 * kLogitsMaxCluster;                          // [2][warps]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kLogitsWarps);
+  uint64_t* empty = full + kLogitsMaxBuffers;
+  uint64_t* xbar = empty + kLogitsMaxBuffers;                          // [2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(xbar + 2);
 
   const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
   const int64_t cluster = blockIdx.x / CL;
   const int64_t nclusters = gridDim.x / CL;
   const int lo = static_cast<int>(rank) * a.Vs;
   const int len = max(0, min(a.V, lo + a.Vs) - lo);  // columns of this slice (multiple of 8)
   const uint32_t bytes = static_cast<uint32_t>(len) * 2u;
-  const int nvec = len / 8;
-  const int K = a.K;
+  const int64_t rows = cluster < a.N ? (a.N - cluster + nclusters - 1) / nclusters : 0;
+  const bool grad = a.dZ != nullptr;
 
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], kLogitsWarps);
+    }
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
   if constexpr (CL > 1)
-    cluster_sync();
+    cluster_sync();  // peers' barriers exist before any st.async reaches them
   else
     __syncthreads();
 
-  auto load_row = [&](int64_t row, int b) {  // thread 0 only
-    mbar_arrive_expect_tx(&full[b], bytes);
-    if (bytes) bulk_load_1d(buf(b), a.Z + row * a.ldz + lo, bytes, &full[b]);
-  };
-  if (tid == 0 && cluster < a.N) load_row(cluster, 0);
-
-  int i = 0;
-  for (int64_t row = cluster; row < a.N; row += nclusters, ++i) {
-    const int b = i & 1;
-    const int64_t next = row + nclusters;
-    if (tid == 0 && next < a.N && !*abort_flag) {
-      if (a.dZ) bulk_wait_group_read<0>();  // the store from the other buffer has read it
-      load_row(next, b ^ 1);
-    }
-    const bool have = mbar_wait_bounded(&full[b], static_cast<uint32_t>((i >> 1) & 1), abort_flag,
-                                        a.timeout_ns, a.status, 6);
-    const bool work = __syncthreads_and(have ? 1 : 0) != 0;
-    const uint16_t* zrow = buf(b);
-
-    // ---- pass 1: online max / sum of exponentials, and the teacher's cross term
-    float2 ms = make_float2(-INFINITY, 0.0f);
-    float cross = 0.0f;
-    int2 pr = make_int2(INT_MAX, 0);
-    float zk = 0.0f;
-    bool mine = false;  // this thread's teacher entry falls in the slice
-    if (work) {
-      for (int v = tid; v < nvec; v += kLogitsThreads) {
-        const uint4 w = *reinterpret_cast<const uint4*>(zrow + 8 * v);
-        float z[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                      bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-        float mx = z[0];
-#pragma unroll
-        for (int j = 1; j < 8; ++j) mx = fmaxf(mx, z[j]);
-        const float mnew = fmaxf(ms.x, mx * a.scale2);
-        float s = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s += ex2_approx(fmaf(z[j], a.scale2, -mnew));
-        ms.y = ms.y * ex2_approx(ms.x - mnew) + s;
-        ms.x = mnew;
-      }
-      if (tid < K) {
-        pr = __ldg(&a.pairs[row * K + tid]);
-        if (pr.x >= lo && pr.x < lo + len) {
-          zk = __uint_as_float(static_cast<uint32_t>(zrow[pr.x - lo]) << 16);
-          cross = __int_as_float(pr.y) * zk;
-          mine = true;
+  if (tid < 32) {
+    // ---------------------------------------------------------------- copy driver
+    if (tid == 0) {
+      auto store = [&](int64_t j, int b) {
+        if (grad && bytes && !*abort_flag) {
+          bulk_store_1d(a.dZ + (cluster + j * nclusters) * a.lddz + lo, buf(b), bytes);
+          bulk_commit_group();
         }
+      };
+      for (int64_t j = 0; j < rows; ++j) {
+        const int b = static_cast<int>(j % NBUF);
+        const int64_t u = j / NBUF;
+        if (u > 0) {
+          // row j - NBUF is finished in this buffer: store its dZ, let the store
+          // read the buffer, then reuse it
+          if (!mbar_wait_bounded(&empty[b], static_cast<uint32_t>((u - 1) & 1), abort_flag,
+                                 a.timeout_ns, a.status, 6))
+            break;
+          store(j - NBUF, b);
+          bulk_wait_group_read<0>();
+        }
+        mbar_arrive_expect_tx(&full[b], bytes);
+        if (bytes) bulk_load_1d(buf(b), a.Z + (cluster + j * nclusters) * a.ldz + lo, bytes, &full[b]);
       }
+      for (int64_t j = rows > NBUF ? rows - NBUF : 0; j < rows && !*abort_flag; ++j) {
+        const int b = static_cast<int>(j % NBUF);
+        if (!mbar_wait_bounded(&empty[b], static_cast<uint32_t>((j / NBUF) & 1), abort_flag,
+                               a.timeout_ns, a.status, 6))
+          break;
+        store(j, b);
+      }
+      bulk_wait_group_all();
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, ms.x, o),
-                                       __shfl_xor_sync(0xffffffffu, ms.y, o));
-      ms = merge_ms(ms, other);
-      cross += __shfl_xor_sync(0xffffffffu, cross, o);
-    }
-    if (lane == 0) red[warp] = make_float4(ms.x, ms.y, cross, 0.0f);
-    __syncthreads();
-    float2 bms = make_float2(-INFINITY, 0.0f);
-    float bcross = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kLogitsWarps; ++w) {
-      const float4 r = red[w];
-      bms = merge_ms(bms, make_float2(r.x, r.y));
-      bcross += r.z;
-    }
+    __syncwarp();  // the warp reconverges before the final cluster barrier
+  } else {
+    // ---------------------------------------------------------------- compute warps
+    const int ctid = tid - 32;
+    const int cwarp = ctid >> 5, lane = ctid & 31;
+    const int nvec = len / 8;
+    const int K = a.K;
+    for (int64_t j = 0; j < rows; ++j) {
+      const int64_t row = cluster + j * nclusters;
+      const int b = static_cast<int>(j % NBUF);
+      const int par = static_cast<int>(j & 1);
+      bool work = !*abort_flag &&
+                  mbar_wait_bounded(&full[b], static_cast<uint32_t>((j / NBUF) & 1), abort_flag,
+                                    a.timeout_ns, a.status, 6);
+      const uint16_t* zrow = buf(b);
 
-    // ---- merge over the cluster (distributed shared memory)
-    float2 rms = bms;
-    float rcross = bcross;
-    if constexpr (CL > 1) {
-      float4* slot = exch + b * kLogitsMaxCluster;
-      if (tid < CL) {
-        const uint32_t dst = mapa_shared(smem_u32(&slot[rank]), static_cast<uint32_t>(tid));
-        st_cluster_v4(dst, make_float4(bms.x, bms.y, bcross, 0.0f));
-      }
-      cluster_sync();
-      rms = make_float2(-INFINITY, 0.0f);
-      rcross = 0.0f;
-#pragma unroll
-      for (int r = 0; r < CL; ++r) {
-        const float4 p = slot[r];
-        rms = merge_ms(rms, make_float2(p.x, p.y));
-        rcross += p.z;
-      }
-    }
-    const float lse2 = rms.x + log2f(rms.y);
-    const bool counted = (a.mask == nullptr) || (a.mask[row] != 0);
-    if (rank == 0 && tid == 0 && work) {
-      const double lse = static_cast<double>(lse2) * 0.6931471805599453;
-      a.lse[row] = static_cast<float>(lse);
-      a.loss[row] = counted ? static_cast<float>(static_cast<double>(a.ent[row]) -
-                                                 static_cast<double>(rcross) * a.inv_T + lse)
-                            : 0.0f;
-    }
-
-    // ---- pass 2: dZ in place, then one bulk store
-    if (a.dZ && work) {
-      const float gs = counted ? a.dloss[row] * a.inv_T : 0.0f;
-      uint16_t* drow = buf(b);
-      for (int v = tid; v < nvec; v += kLogitsThreads) {
-        uint4* p = reinterpret_cast<uint4*>(drow + 8 * v);
-        uint4 w = *p;
-        if (counted) {
+      // ---- pass 1: online max / sum of exponentials, and the teacher's cross term
+      float2 ms = make_float2(-INFINITY, 0.0f);
+      float cross = 0.0f;
+      int2 pr = make_int2(INT_MAX, 0);
+      float zk = 0.0f;
+      bool mine = false;  // this thread's teacher entry falls in the slice
+      if (work) {
+        for (int v = ctid; v < nvec; v += kLogitsThreads) {
+          const uint4 w = *reinterpret_cast<const uint4*>(zrow + 8 * v);
           const float z[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                               bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-          float d[8];
+          float mx = z[0];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) d[j] = gs * ex2_approx(fmaf(z[j], a.scale2, -lse2));
-          w = make_uint4(f2_to_bf16x2(d[0], d[1]), f2_to_bf16x2(d[2], d[3]),
-                         f2_to_bf16x2(d[4], d[5]), f2_to_bf16x2(d[6], d[7]));
-        } else {
-          w = make_uint4(0u, 0u, 0u, 0u);
+          for (int i = 1; i < 8; ++i) mx = fmaxf(mx, z[i]);
+          const float mnew = fmaxf(ms.x, mx * a.scale2);
+          float s = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s += ex2_approx(fmaf(z[i], a.scale2, -mnew));
+          ms.y = ms.y * ex2_approx(ms.x - mnew) + s;
+          ms.x = mnew;
         }
-        *p = w;
-      }
-      __syncthreads();
-      if (counted && mine && (tid == 0 || __ldg(&a.pairs[row * K + tid - 1]).x != pr.x)) {
-        float P = __int_as_float(pr.y);  // merge a run of repeated ids
-        for (int k2 = tid + 1; k2 < K; ++k2) {
-          const int2 q = __ldg(&a.pairs[row * K + k2]);
-          if (q.x != pr.x) break;
-          P += __int_as_float(q.y);
+        if (ctid < K) {
+          pr = __ldg(&a.pairs[row * K + ctid]);
+          if (pr.x >= lo && pr.x < lo + len) {
+            zk = __uint_as_float(static_cast<uint32_t>(zrow[pr.x - lo]) << 16);
+            cross = __int_as_float(pr.y) * zk;
+            mine = true;
+          }
         }
-        const float d = gs * (ex2_approx(fmaf(zk, a.scale2, -lse2)) - P);
-        const __nv_bfloat16 h = __float2bfloat16_rn(d);
-        drow[pr.x - lo] = *reinterpret_cast<const uint16_t*>(&h);
       }
-      fence_proxy_async_shared();
-      __syncthreads();
-      if (tid == 0 && bytes) {
-        bulk_store_1d(a.dZ + row * a.lddz + lo, drow, bytes);
-        bulk_commit_group();
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, ms.x, o),
+                                         __shfl_xor_sync(0xffffffffu, ms.y, o));
+        ms = merge_ms(ms, other);
+        cross += __shfl_xor_sync(0xffffffffu, cross, o);
       }
+      float4* rd = red + par * kLogitsWarps;
+      if (lane == 0) rd[cwarp] = make_float4(ms.x, ms.y, cross, 0.0f);
+      compute_sync();
+      float2 rms = make_float2(-INFINITY, 0.0f);
+      float rcross = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kLogitsWarps; ++w) {
+        const float4 r = rd[w];
+        rms = merge_ms(rms, make_float2(r.x, r.y));
+        rcross += r.z;
+      }
+
+      // ---- merge over the cluster: every CTA sends its partial to every CTA
+      if constexpr (CL > 1) {
+        float4* slot = exch + par * kLogitsMaxCluster;
+        if (ctid == 0) mbar_arrive_expect_tx(&xbar[par], CL * 16);
+        if (ctid < CL) {
+          const uint32_t dst = mapa_shared(smem_u32(&slot[rank]), static_cast<uint32_t>(ctid));
+          const uint32_t bar = mapa_shared(smem_u32(&xbar[par]), static_cast<uint32_t>(ctid));
+          st_async_v4(dst, make_float4(rms.x, rms.y, rcross, 0.0f), bar);
+        }
+        work = mbar_wait_bounded(&xbar[par], static_cast<uint32_t>((j >> 1) & 1), abort_flag,
+                                 a.timeout_ns, a.status, 6) && work;
+        rms = make_float2(-INFINITY, 0.0f);
+        rcross = 0.0f;
+#pragma unroll
+        for (int r = 0; r < CL; ++r) {
+          const float4 q = slot[r];
+          rms = merge_ms(rms, make_float2(q.x, q.y));
+          rcross += q.z;
+        }
+      }
+      const float lse2 = rms.x + log2f(rms.y);
+      const bool counted = (a.mask == nullptr) || (a.mask[row] != 0);
+      if (rank == 0 && ctid == 0 && work) {
+        const double lse = static_cast<double>(lse2) * 0.6931471805599453;
+        a.lse[row] = static_cast<float>(lse);
+        a.loss[row] = counted ? static_cast<float>(static_cast<double>(a.ent[row]) -
+                                                   static_cast<double>(rcross) * a.inv_T + lse)
+                              : 0.0f;
+      }
+
+      // ---- pass 2: dZ in place (the copy driver stores it)
+      if (grad && work) {
+        const float gs = counted ? a.dloss[row] * a.inv_T : 0.0f;
+        uint16_t* drow = buf(b);
+        for (int v = ctid; v < nvec; v += kLogitsThreads) {
+          uint4* p = reinterpret_cast<uint4*>(drow + 8 * v);
+          uint4 w = *p;
+          if (counted) {
+            const float z[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+            float d[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d[i] = gs * ex2_approx(fmaf(z[i], a.scale2, -lse2));
+            w = make_uint4(f2_to_bf16x2(d[0], d[1]), f2_to_bf16x2(d[2], d[3]),
+                           f2_to_bf16x2(d[4], d[5]), f2_to_bf16x2(d[6], d[7]));
+          } else {
+            w = make_uint4(0u, 0u, 0u, 0u);
+          }
+          *p = w;
+        }
+        compute_sync();  // the vectors are written before single entries are corrected
+        if (counted && mine && (ctid == 0 || __ldg(&a.pairs[row * K + ctid - 1]).x != pr.x)) {
+          float P = __int_as_float(pr.y);  // merge a run of repeated ids
+          for (int k2 = ctid + 1; k2 < K; ++k2) {
+            const int2 q = __ldg(&a.pairs[row * K + k2]);
+            if (q.x != pr.x) break;
+            P += __int_as_float(q.y);
+          }
+          const float d = gs * (ex2_approx(fmaf(zk, a.scale2, -lse2)) - P);
+          const __nv_bfloat16 h = __float2bfloat16_rn(d);
+          drow[pr.x - lo] = *reinterpret_cast<const uint16_t*>(&h);
+        }
+        fence_proxy_async_shared();  // the copy engine reads what these threads wrote
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[b]);
     }
-    __syncthreads();  // this buffer is free for the row after next
   }
 
-  if (tid == 0) bulk_wait_group_all();
   if (*abort_flag) {
     // copies issued before giving up land within microseconds
     const uint64_t t0 = globaltimer_ns();

@@ -99,6 +99,15 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float4 v) {
                : "memory");
 }
 
+// Store 16 bytes into a (possibly remote) CTA's shared memory and count them
+// on that CTA's mbarrier (complete_tx); both are shared::cluster addresses.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float4 v, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(cluster_addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cluster_bar)
+      : "memory");
+}
+
 // All threads of all CTAs of the cluster.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
