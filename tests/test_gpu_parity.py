@@ -208,7 +208,7 @@ def test_gptoss_head_long_sweep(N):
 def test_peak_memory_linear_in_tokens():
     D, V, K = 2880, 201088, 64
     peaks = []
-    Ns = [4096, 16384, 65536]
+    Ns = [8192, 32768, 65536]  # every N holds two backward chunks (one dW group)
     for N in Ns:
         p = make_problem(N, D, V, K, 1.0, seed=20, device=DEV)
         torch.cuda.synchronize()

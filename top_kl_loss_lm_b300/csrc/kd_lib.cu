@@ -190,7 +190,13 @@ struct Layout {
   int slots = 0;
   int64_t C = 0, C_pad = 0, dz_ld = 0;
   int NB = 0;
+  int G = 1;  // backward chunks per dW launch (dZ slots kept at once)
 };
+
+// Backward chunks whose dZ is kept together so that one dW launch contracts over
+// all their tokens: half as many read-add-write passes over the fp32 dW.
+constexpr int kDwGroup = 2;
+constexpr int kMaxDwGroup = 4;
 
 Layout plan(int64_t N, int D, int V, int K, int64_t chunk) {
   Layout L;
@@ -218,8 +224,9 @@ Layout plan(int64_t N, int D, int V, int K, int64_t chunk) {
   L.C = C;
   L.C_pad = C;
   L.dz_ld = static_cast<int64_t>(L.NB) * kBNMax;
+  L.G = static_cast<int>(cdiv(N, C) < kDwGroup ? (cdiv(N, C) < 1 ? 1 : cdiv(N, C)) : kDwGroup);
   L.dz = off;
-  off = align256(off + static_cast<size_t>(L.C_pad) * L.dz_ld * sizeof(uint16_t));
+  off = align256(off + static_cast<size_t>(L.G) * L.C_pad * L.dz_ld * sizeof(uint16_t));
   L.dhp = off;  // k-split partials of dH take whatever follows (sized at call time)
   L.bwd_end = off;
   L.total = L.fwd_end > L.bwd_end ? L.fwd_end : L.bwd_end;
@@ -442,18 +449,24 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
 
   const int BNd = hidden_tile_width(D);
   const int NBd = static_cast<int>(cdiv(D, BNd));
-  CUtensorMap mH_k, mW_k, mDz_k, mW_mn, mDz_mn, mH_mn;
+  if (L.G < 1 || L.G > kMaxDwGroup) return KD_ERR_UNSUPPORTED;
+  CUtensorMap mH_k, mW_k, mW_mn, mDz_mn, mH_mn;
+  CUtensorMap mDz_k[kMaxDwGroup], mDz_out[kMaxDwGroup];  // one per dZ slot
   const uint64_t rowH = static_cast<uint64_t>(D) * 2;
   const uint64_t rowDz = static_cast<uint64_t>(L.dz_ld) * 2;
+  const int64_t slot_elems = L.C_pad * L.dz_ld;
   if (!make_map(&mH_k, H, D, N, rowH, kBK, kBM) ||
       !make_map(&mW_k, W, D, V, rowH, kBK, Geo<kPair>::kBRows) ||
-      !make_map(&mDz_k, dz, V, L.C_pad, rowDz, kBK, kBM) ||
-      !make_map(&mW_mn, W, D, V, rowH, 64, kBK) || !make_map(&mDz_mn, dz, V, L.C_pad, rowDz, 64, kBK) ||
+      !make_map(&mW_mn, W, D, V, rowH, 64, kBK) ||
+      !make_map(&mDz_mn, dz, V, static_cast<uint64_t>(L.G) * L.C_pad, rowDz, 64, kBK) ||
       !make_map(&mH_mn, H, D, N, rowH, 64, kBK))
     return KD_ERR_CUDA;
-  CUtensorMap mDw_out, mDhp_out, mDz_out;
+  for (int g = 0; g < L.G; ++g)
+    if (!make_map(&mDz_k[g], dz + g * slot_elems, V, L.C_pad, rowDz, kBK, kBM) ||
+        !make_out_map(&mDz_out[g], dz + g * slot_elems, V, L.C_pad, rowDz, true))
+      return KD_ERR_CUDA;
+  CUtensorMap mDw_out, mDhp_out;
   if (!make_out_map(&mDw_out, dW, D, V, static_cast<uint64_t>(D) * 4) ||
-      !make_out_map(&mDz_out, dz, V, L.C_pad, rowDz, true) ||
       (KS > 1 && !make_out_map(&mDhp_out, dhp, D, static_cast<uint64_t>(KS) * L.C_pad,
                                static_cast<uint64_t>(D) * 4)))
     return KD_ERR_CUDA;
@@ -462,7 +475,11 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
   const int KBd = static_cast<int>(cdiv(D, kBK));
   const int KBv = static_cast<int>(cdiv(V, kBK));
   const int MBv = static_cast<int>(cdiv(V, kTileRows));
-  for (int64_t c0 = 0; c0 < N; c0 += L.C) {
+  const int64_t group = static_cast<int64_t>(L.G) * L.C;
+  for (int64_t g0 = 0; g0 < N; g0 += group) {
+   const int64_t group_rows = (N - g0) < group ? (N - g0) : group;
+   for (int slot = 0; slot < L.G && g0 + slot * L.C < N; ++slot) {
+    const int64_t c0 = g0 + slot * L.C;
     const int64_t rows = (N - c0) < L.C ? (N - c0) : L.C;
     const int MBc = static_cast<int>(cdiv(rows, kTileRows));
 
@@ -486,7 +503,8 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     a.dz_ld = L.dz_ld;
     {
       ProfScope ps(kProfDzGemm, s);
-      if ((st = launch_gemm<kEpiDz, false, false, kPair>(mH_k, mW_k, mDz_out, a, di, s)) != KD_OK)
+      if ((st = launch_gemm<kEpiDz, false, false, kPair>(mH_k, mW_k, mDz_out[slot], a, di, s)) !=
+          KD_OK)
         return st;
     }
 
@@ -504,7 +522,8 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
     h.out_slot_rows = static_cast<int>(L.C_pad);
     {
       ProfScope ps(kProfDhGemm, s);
-      if ((st = launch_gemm<kEpiDh, false, true, kPair>(mDz_k, mW_mn, mDhp_out, h, di, s)) != KD_OK)
+      if ((st = launch_gemm<kEpiDh, false, true, kPair>(mDz_k[slot], mW_mn, mDhp_out, h, di, s)) !=
+          KD_OK)
         return st;
     }
     if (h.sched.KS > 1) {
@@ -517,17 +536,20 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
       if ((st = cuda_check()) != KD_OK) return st;
     }
 
-    // 3. dW (+)= dZ^T H over the chunk's tokens
+   }
+    // 3. dW (+)= dZ^T H over the group's tokens: slot g's rows are tokens
+    //    g0 + g*C + t, so the stacked slots are the group's tokens in order (rows
+    //    past the end of a short last chunk were stored as zeros)
     GemmArgs g = base_args(di);
-    g.sched = make_tile_sched(MBv, NBd, static_cast<int>(cdiv(rows, kBK)), 1);
+    g.sched = make_tile_sched(MBv, NBd, static_cast<int>(cdiv(group_rows, kBK)), 1);
     g.M = V;
     g.Ncols = D;
     g.BN = BNd;
     g.idesc = umma_idesc_bf16(kTileRows, BNd, true, true);
-    g.b_k_off = static_cast<int>(c0);
+    g.b_k_off = static_cast<int>(g0);
     g.out_f32 = dW;
     g.ld_out = D;
-    g.accumulate = (c0 > 0 || accumulate_dW) ? 1 : 0;
+    g.accumulate = (g0 > 0 || accumulate_dW) ? 1 : 0;
     {
       ProfScope ps(kProfDwGemm, s);
       if ((st = launch_gemm<kEpiDw, true, true, kPair>(mDz_mn, mH_mn, mDw_out, g, di, s)) != KD_OK)
