@@ -8,4 +8,5 @@ from .kd_oracle import (  # noqa: F401
     mean_loss,
     student_logits,
     teacher_log_probs,
+    teacher_topk,
 )

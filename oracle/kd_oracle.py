@@ -47,6 +47,7 @@ __all__ = [
     "mean_loss",
     "dense_teacher_grid",
     "kd_from_logits",
+    "teacher_topk",
 ]
 
 
@@ -202,3 +203,28 @@ def kd_from_logits(Z, idx, t, mask, T: float, g=None, row_chunk: int = 64):
             gv = np.asarray(g, dtype=np.float64)[r0 + valid]
             dZ[r0 + valid] = (gv / T)[:, None] * (np.exp(log_q) - P)
     return loss, lse, int(mask.sum()), dZ
+
+
+def teacher_topk(H, W, K: int, row_chunk: int = 64):
+    """The teacher's cached top-K: per row, the K largest logits of H W^T and their ids.
+
+    Offline distillation caches, once per training position, the teacher's K most
+    likely tokens and their logits, so the teacher never has to be resident while
+    the student trains (blog "Two systems changes", offline-distillation paragraph;
+    the pages' cache holds the top 100). Per row n (fp64, exact bf16 inputs):
+      z = H[n] W^T;  ids = the K positions of the largest z, in descending order of z
+    Ties at the boundary make several id sets correct; this returns the one a
+    stable descending sort gives (lower id first among equal logits).
+    Returns (ids[N, K] int64, logits[N, K] fp64).
+    """
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    N = H.shape[0]
+    ids = np.zeros((N, K), dtype=np.int64)
+    vals = np.zeros((N, K), dtype=np.float64)
+    for r0, r1 in _blocks(N, row_chunk):
+        z = student_logits(H[r0:r1], W)
+        order = np.argsort(-z, axis=1, kind="stable")[:, :K]
+        ids[r0:r1] = order
+        vals[r0:r1] = np.take_along_axis(z, order, axis=1)
+    return ids, vals

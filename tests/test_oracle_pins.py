@@ -371,3 +371,35 @@ def test_logits_form_finite_differences():
                 Zm = Z.copy(); Zm[i, j] -= h
                 num[i, j] = (f(Zp) - f(Zm)) / (2 * h)
         assert _rel(dZ, num) < 1e-7
+
+
+# ----------------------------------------------------------------------------- teacher top-K cache
+
+
+def test_teacher_topk_brute_force_and_invariants():
+    rng = np.random.default_rng(31)
+    H = rng.standard_normal((5, 6))
+    W = rng.standard_normal((40, 6))
+    W[7] = W[3]  # two tokens with equal logits in every row
+    K = 9
+    ids, vals = oracle.teacher_topk(H, W, K, row_chunk=2)
+    for n in range(H.shape[0]):
+        z = [float(sum(H[n, d] * W[j, d] for d in range(6))) for j in range(40)]
+        ranked = sorted(range(40), key=lambda j: (-z[j], j))  # brute force, python sort
+        assert list(ids[n]) == ranked[:K]
+        assert np.allclose(vals[n], [z[j] for j in ranked[:K]], rtol=0, atol=1e-12)
+        assert np.all(np.diff(vals[n]) <= 0)
+        rest = np.delete(np.array(z), ids[n])
+        assert rest.max() <= vals[n, -1]
+    # K = V returns a full descending permutation
+    ids_all, vals_all = oracle.teacher_topk(H[:2], W, 40)
+    assert sorted(ids_all[0]) == list(range(40))
+
+
+def test_teacher_topk_feeds_the_loss_at_k_equals_v():
+    # caching all V logits and distilling from the cache is the exact dense KL:
+    # with the student equal to the teacher the loss is zero
+    H, W, _, _, _ = _rand_problem(32, 3, 5, 11, 1)
+    ids, vals = oracle.teacher_topk(H, W, 11)
+    loss, _, _ = oracle.kd_forward(H, W, ids, vals, np.ones(3, dtype=np.uint8), 1.3)
+    assert np.max(np.abs(loss)) < 1e-12
