@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--logits", action="store_true",
                     help="measure the loss from materialised logits (kd_topk_kl_logits) instead")
     ap.add_argument("--logits-rows", type=int, default=32768)
+    ap.add_argument("--teacher-topk", action="store_true",
+                    help="measure the teacher top-K cache producer (kd_teacher_topk) instead")
     ap.add_argument("--traffic-from", default=None,
                     help="write the per-launch DRAM traffic record from this ncu --csv log and exit")
     return ap.parse_args()
@@ -60,7 +62,7 @@ def parse():
 
 def traffic_file(workload: str) -> str:
     return os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.json")
-KERNEL_SOURCES = ("kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h", "kd_logits.cuh")
+KERNEL_SOURCES = ("kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h", "kd_logits.cuh", "kd_topk_cache.cuh")
 # template argument of kd_gemm_kernel -> category of the library's launch timing
 GEMM_EPI = {"0": "fwd_gemm", "1": "dz_gemm", "2": "dh_gemm", "3": "dw_gemm"}
 
@@ -619,6 +621,100 @@ def run_logits(args):
     return 0
 
 
+TOPK_METRIC = "teacher top-K cache (logit GEMM + exact per-row top-K): rows/s; GEMM TFLOP/s"
+
+
+def run_teacher_topk(args):
+    """The offline step: the teacher's top-K ids and logits of H W^T for N rows."""
+    import torch
+
+    from top_kl_loss_lm_b300 import binding
+    from workloads import make_problem
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    N, D, V = args.logits_rows, 2880, 201088
+    K = args.K or 100
+    p = make_problem(N, D, V, 1, 1.0, seed=args.seed, device=dev, name="gptoss_teacher")
+    ws = torch.empty(binding.kd_teacher_topk_workspace_size(N, D, V, K), dtype=torch.uint8,
+                     device=dev)
+    ids = torch.empty(N, K, dtype=torch.int32, device=dev)
+    vals = torch.empty(N, K, device=dev)
+
+    def step():
+        binding.kd_teacher_topk(p.H, p.W, ids, vals, ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if binding.kd_get_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    sampler = ClockSampler(0)
+    torch.cuda.synchronize()
+    sampler.start()
+    binding.kd_debug_profile(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    prof = binding.kd_debug_profile_read()
+    binding.kd_debug_profile(False)
+    if binding.kd_get_status() != 0:
+        raise RuntimeError("device status in the timed region")
+    ms = e0.elapsed_time(e1)
+    gemm_ms = prof["topk_gemm"][0] / args.steps
+    sel_ms = prof["topk_select"][0] / args.steps
+    flops = 2.0 * N * D * V
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = flops / (gemm_ms / 1000.0) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline:
+        import numpy as np
+
+        import oracle
+        W64 = p.W.double().cpu().numpy()
+        rng = np.random.default_rng(args.seed)
+        done, secs = 0, 0.0
+        while secs < args.cpu_seconds and done < 4096:
+            rows = np.sort(rng.choice(N, size=64, replace=False))
+            Hs = p.H[torch.as_tensor(rows, device=dev)].double().cpu().numpy()
+            t0 = time.perf_counter()
+            oracle.teacher_topk(Hs, W64, K)
+            secs += time.perf_counter() - t0
+            done += len(rows)
+        try:
+            from threadpoolctl import threadpool_info
+            threads = max(int(d.get("num_threads", 1)) for d in threadpool_info())
+        except Exception:
+            threads = os.cpu_count()
+        cpu = {"value": done / secs, "unit": "rows/s", "cores": threads, "kind": "oracle",
+               "sample": f"{done} seeded rows of {N} in 64-row calls ({secs:.1f} s)"}
+    line = {
+        "metric": TOPK_METRIC, "value": args.steps * N / (ms / 1000.0), "unit": "rows/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"gptoss_teacher: N={N} rows, D={D}, V={V}, K={K}",
+                   "N": N, "D": D, "V": V, "K": K,
+                   "l2": "inputs larger than L2 (W alone is 1.16 GB)",
+                   "inputs": "H ~ N(0,1), W ~ N(0,1/D) in bf16"},
+        "roofline": {"bound": "tensor", "kernel": "topk_gemm", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": recorded_traffic("topk_gemm", "gptoss_teacher", 0),
+                     "peak_kind": f"sustained bf16 dense ({src})", "flops_per_step": flops},
+        "kernels": {"topk_gemm": {"ms_per_step": gemm_ms}, "topk_select": {"ms_per_step": sel_ms}},
+        "gpu_launches": int(sum(c[1] for c in prof.values())),
+        "clocks": clocks, "e2e": None, "cpu_baseline": cpu,
+        "note": "secondary line (the upstream caching step); e2e omitted",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_sweep(args):
     """Peak device memory and rate vs N (D, V, K of the gpt-oss head)."""
     import torch
@@ -667,6 +763,8 @@ def main():
         return run_sweep(args)
     if args.logits:
         return run_logits(args)
+    if args.teacher_topk:
+        return run_teacher_topk(args)
     return run_ours(args, rank, world, local)
 
 

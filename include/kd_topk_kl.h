@@ -133,6 +133,28 @@ kd_status kd_topk_kl_logits(const uint16_t* Z, int64_t ldz, const int32_t* topk_
                             size_t ws_bytes, kd_stream_t stream);
 
 /*
+ * The teacher's top-K cache: per row, the K largest logits of Z = H W^T and
+ * their token ids, in descending order of logit (ties: lower id first). This
+ * is the offline step of the method (blog "Making Knowledge Distillation Cheap
+ * Enough to Run at Scale", section "Two systems changes", offline-distillation
+ * paragraph: the teacher's top-K logits are cached once so the teacher never
+ * has to be resident while the student trains; the pages cache the top 100).
+ * Its output is the topk_idx / topk_logit input of the loss calls above.
+ *   H [N x D] bf16 teacher hidden states, W [V x D] bf16 teacher lm-head weight.
+ *   topk_idx [N x K] int32, topk_logit [N x K] fp32 outputs (raw logits; the
+ *   loss applies the temperature).
+ *   ws: kd_teacher_topk_workspace_size(N, D, V, K) bytes (one chunk of at most
+ *   4,096 rows of fp32 logits, fixed in N beyond that).
+ * D a multiple of 8, 1 <= K <= min(V, 256). The logits are accumulated in fp32
+ * on the tensor cores and the selection is exact on those fp32 values.
+ */
+size_t kd_teacher_topk_workspace_size(int64_t N, int D, int V, int K);
+
+kd_status kd_teacher_topk(const uint16_t* H, const uint16_t* W, int64_t N, int D, int V, int K,
+                          int32_t* topk_idx, float* topk_logit, void* ws, size_t ws_bytes,
+                          kd_stream_t stream);
+
+/*
  * Forward with no workspace argument and no allocation, for callers that
  * cannot obtain device memory themselves (a plugin inside a process whose own
  * allocator already holds the GPU's memory, or a hot path where cudaMalloc,

@@ -19,6 +19,7 @@ __all__ = [
     "KdError", "lib", "library_path",
     "kd_topk_kl_workspace_size", "kd_topk_kl_fwd", "kd_topk_kl_bwd", "kd_topk_kl_fwd_noalloc",
     "kd_topk_kl_logits_workspace_size", "kd_topk_kl_logits",
+    "kd_teacher_topk_workspace_size", "kd_teacher_topk",
     "kd_get_status", "kd_status_string",
     "kd_debug_gemm_bf16", "kd_debug_wait_timeout", "kd_debug_schedule",
     "kd_debug_profile", "kd_debug_profile_read", "PROFILE_CATEGORIES",
@@ -71,6 +72,10 @@ def lib() -> ctypes.CDLL:
         L.kd_topk_kl_logits.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, f32, vp, vp, vp, vp,
                                         i64, vp, sz, vp]
         L.kd_topk_kl_logits.restype = i32
+        L.kd_teacher_topk_workspace_size.argtypes = [i64, i32, i32, i32]
+        L.kd_teacher_topk_workspace_size.restype = sz
+        L.kd_teacher_topk.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, vp, sz, vp]
+        L.kd_teacher_topk.restype = i32
         L.kd_get_status.argtypes = [vp]
         L.kd_get_status.restype = i32
         L.kd_status_string.argtypes = [i32]
@@ -222,6 +227,26 @@ def kd_topk_kl_logits(Z, topk_idx, topk_logit, mask, T: float, loss, lse, n_vali
     _check(lib().kd_topk_kl_logits(*args), "kd_topk_kl_logits")
 
 
+def kd_teacher_topk_workspace_size(N: int, D: int, V: int, K: int) -> int:
+    return int(lib().kd_teacher_topk_workspace_size(N, D, V, K))
+
+
+def kd_teacher_topk(H, W, topk_idx, topk_logit, ws, stream=None):
+    """The teacher's top-K cache (ids int32, logits fp32) of H W^T into caller tensors."""
+    N, D = H.shape
+    V = W.shape[0]
+    K = topk_idx.shape[1]
+    dev = H.device
+    args = (
+        _ptr(H, torch.bfloat16, (N, D), "H", dev), _ptr(W, torch.bfloat16, (V, D), "W", dev),
+        N, D, V, K,
+        _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
+        _ptr(topk_logit, torch.float32, (N, K), "topk_logit", dev),
+        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream),
+    )
+    _check(lib().kd_teacher_topk(*args), "kd_teacher_topk")
+
+
 def kd_get_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
     return int(lib().kd_get_status(_stream(stream)))
@@ -268,7 +293,7 @@ def kd_debug_schedule(kind: int, rows: int, cols: int, depth: int, grid_units: i
 
 
 PROFILE_CATEGORIES = ["prep", "fwd_gemm", "combine", "dz_gemm", "dh_gemm", "dh_sum", "dw_gemm",
-                      "logits"]
+                      "logits", "topk_gemm", "topk_select"]
 
 
 def kd_debug_profile(enable: bool):

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libkdtopk.so")
 SOURCES = ["kd_lib.cu"]
-DEPENDS = ["kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h", "kd_logits.cuh"]
+DEPENDS = ["kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h", "kd_logits.cuh", "kd_topk_cache.cuh"]
 HEADERS = [os.path.join(os.path.dirname(HERE), "include", h)
            for h in ("kd_topk_kl.h", "kd_topk_kl_testing.h")]
 

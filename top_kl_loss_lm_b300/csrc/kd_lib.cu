@@ -22,6 +22,7 @@
 #include "kd_aux.cuh"
 #include "kd_gemm.cuh"
 #include "kd_logits.cuh"
+#include "kd_topk_cache.cuh"
 #include "kd_sched.h"
 
 namespace kd {
@@ -51,7 +52,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // Optional per-launch timing (test hook kd_debug_profile): a start/stop event
 // pair recorded on the launching stream around every kernel of the library.
 enum ProfCat : int { kProfPrep = 0, kProfFwdGemm, kProfCombine, kProfDzGemm, kProfDhGemm, kProfDhSum,
-                     kProfDwGemm, kProfLogits, kProfCats };
+                     kProfDwGemm, kProfLogits, kProfTopkGemm, kProfTopkSelect, kProfCats };
 struct Prof {
   bool on = false;
   std::vector<cudaEvent_t> ev;      // pool: 2 per record
@@ -699,6 +700,74 @@ extern "C" kd_status kd_topk_kl_logits(const uint16_t* Z, int64_t ldz, const int
     case 4: return launch_logits<4, 2>(a, di, s);
     default: return launch_logits<8, 2>(a, di, s);
   }
+}
+
+// ------------------------------------------------------------------ teacher top-K cache
+
+namespace kd {
+namespace {
+// Rows of teacher logits materialised at a time (fp32, one chunk of the workspace).
+int64_t topk_chunk_rows(int64_t N) {
+  const int64_t c = 16 * static_cast<int64_t>(kTileRows);  // 4,096
+  return N < c ? cdiv(N < 1 ? 1 : N, kTileRows) * kTileRows : c;
+}
+inline int64_t topk_ld(int V) { return cdiv(V, 8) * 8; }
+}  // namespace
+}  // namespace kd
+
+extern "C" size_t kd_teacher_topk_workspace_size(int64_t N, int D, int V, int K) {
+  if (N < 0 || D <= 0 || D % 8 != 0 || V <= 0 || K < 1 || K > kSelectMaxK || K > V) return 0;
+  return align256(static_cast<size_t>(topk_chunk_rows(N)) * topk_ld(V) * sizeof(float));
+}
+
+extern "C" kd_status kd_teacher_topk(const uint16_t* H, const uint16_t* W, int64_t N, int D, int V,
+                                     int K, int32_t* topk_idx, float* topk_logit, void* ws,
+                                     size_t ws_bytes, kd_stream_t stream) {
+  if (N < 0 || D <= 0 || V <= 0 || K < 1 || K > kSelectMaxK || K > V || D % 8 != 0)
+    return KD_ERR_ARG;
+  if (N > (int64_t(1) << 31) - kBM || V > (1 << 30)) return KD_ERR_UNSUPPORTED;
+  if (N == 0) return KD_OK;
+  if (!H || !W || !topk_idx || !topk_logit || !ws) return KD_ERR_ARG;
+  if (!aligned(H, 16) || !aligned(W, 16) || !aligned(ws, 256) || !aligned(topk_idx, 4) ||
+      !aligned(topk_logit, 4))
+    return KD_ERR_ALIGN;
+  if (ws_bytes < kd_teacher_topk_workspace_size(N, D, V, K)) return KD_ERR_WORKSPACE;
+  kd_status st = KD_OK;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t C = topk_chunk_rows(N);
+  const int64_t ldz = topk_ld(V);
+  float* Zc = static_cast<float*>(ws);
+  CUtensorMap mH, mW, mZ;
+  if (!make_map(&mH, H, D, N, static_cast<uint64_t>(D) * 2, kBK, kBM) ||
+      !make_map(&mW, W, D, V, static_cast<uint64_t>(D) * 2, kBK, Geo<kPair>::kBRows) ||
+      !make_out_map(&mZ, Zc, V, C, static_cast<uint64_t>(ldz) * 4))
+    return KD_ERR_CUDA;
+  const int NB = static_cast<int>(cdiv(V, kBNMax));
+  const int KB = static_cast<int>(cdiv(D, kBK));
+  for (int64_t c0 = 0; c0 < N; c0 += C) {
+    const int64_t rows = (N - c0) < C ? (N - c0) : C;
+    GemmArgs a = base_args(di);
+    a.sched = make_panel_sched(static_cast<int>(cdiv(rows, kTileRows)), NB, KB, gemm_slots(di));
+    a.M = static_cast<int>(rows);
+    a.Ncols = V;
+    a.BN = kBNMax;
+    a.idesc = umma_idesc_bf16(kTileRows, kBNMax, false, false);
+    a.a_row_off = static_cast<int>(c0);
+    {
+      ProfScope ps(kProfTopkGemm, s);
+      if ((st = launch_gemm<kEpiPlain, false, false, kPair>(mH, mW, mZ, a, di, s)) != KD_OK)
+        return st;
+    }
+    int64_t grid = 4L * di->num_sms;
+    if (grid > rows) grid = rows;
+    ProfScope ps(kProfTopkSelect, s);
+    kd_topk_select_kernel<<<static_cast<unsigned>(grid), kSelectThreads, 0, s>>>(
+        Zc, ldz, rows, V, K, topk_idx + c0 * K, topk_logit + c0 * K);
+    if ((st = cuda_check()) != KD_OK) return st;
+  }
+  return KD_OK;
 }
 
 extern "C" kd_status kd_get_status(kd_stream_t stream) {

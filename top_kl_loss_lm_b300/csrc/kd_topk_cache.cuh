@@ -1,0 +1,268 @@
+// kd_topk_cache.cuh — exact per-row top-K of fp32 logits: the selection half of
+// the teacher's top-K cache (the logits come from the tcgen05 GEMM, one chunk of
+// rows at a time).
+//
+// One CTA per row (persistent over the chunk's rows). The K-th largest value is
+// found exactly by a three-level radix select on an order-preserving 32-bit key
+// (11, 11 and 10 bits): each level histograms, in shared memory, the keys whose
+// higher bits match the prefix found so far and picks the bin that holds the
+// K-th largest. A last pass collects every element above that key and as many
+// equal to it as are still needed, and a bitonic sort orders the K of them
+// (descending logit, then ascending id).
+//
+// The row is normally read once. A strided sample of the row (every 64th logit,
+// or sparser so that it fits in shared memory) is selected first, in shared
+// memory, to a key tau0 that about K + 8 sample strides' worth of logits exceed; one pass over the row copies every logit at or above tau0
+// (a few hundred) to shared memory, and the exact radix select and the sort
+// then run there. If that set holds fewer than K logits or more than
+// kSelectCand (heavily tied logits), the row is selected directly: the first
+// radix level reads the row, keeps the logits at or above its chosen bin in
+// shared memory when they fit, and otherwise every level reads the row again.
+#pragma once
+
+#include <cstdint>
+
+namespace kd {
+
+constexpr int kSelectThreads = 512;
+constexpr int kSelectWarps = kSelectThreads / 32;
+constexpr int kSelectBins = 2048;
+constexpr int kSelectMaxK = 256;
+constexpr int kSelectCand = 3072;  // candidates kept in shared memory
+constexpr int kSampleStride = 64;  // the threshold sample takes at most every 64th logit
+
+// Larger float -> larger key (sign flipped for positives, all bits for negatives).
+__device__ __forceinline__ uint32_t float_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Add 1 to hist[bin] for every active lane, one shared atomic per distinct bin.
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active) {
+  const uint32_t live = __ballot_sync(0xffffffffu, active);
+  if (!active) return;
+  const uint32_t peers = __match_any_sync(live, bin);
+  if ((__ffs(peers) - 1) == static_cast<int>(threadIdx.x & 31)) atomicAdd(&hist[bin], __popc(peers));
+}
+
+__global__ void __launch_bounds__(kSelectThreads)
+    kd_topk_select_kernel(const float* __restrict__ Z, int64_t ldz, int64_t rows, int V, int K,
+                          int32_t* __restrict__ out_idx, float* __restrict__ out_val) {
+  __shared__ uint32_t hist[kSelectBins];
+  __shared__ uint32_t warp_sum[kSelectWarps];
+  __shared__ uint32_t s_bin, s_above;
+  __shared__ uint32_t n_gt, n_eq, n_cand;
+  __shared__ uint32_t ckey[kSelectMaxK];
+  __shared__ int32_t cidx[kSelectMaxK];
+  __shared__ uint32_t cand_key[kSelectCand];
+  __shared__ int32_t cand_idx[kSelectCand];
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nvec = V / 4;  // float4 part of the row; the tail (V % 4) is read singly
+
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const float* z = Z + row * ldz;
+    bool in_smem = false;  // the candidates are in cand_key / cand_idx
+
+    // Calls fn(key, id, valid) for every element of the source with warp-uniform
+    // trip counts (fn may use warp-collective operations).
+    auto for_each = [&](auto&& fn) {
+      if (in_smem) {
+        const int n = static_cast<int>(n_cand);
+        for (int base = warp * 32; base < n; base += kSelectThreads) {
+          const int i = base + lane;
+          const bool ok = i < n;
+          fn(ok ? cand_key[i] : 0u, ok ? cand_idx[i] : 0, ok);
+        }
+        return;
+      }
+      for (int base = warp * 32; base < nvec; base += kSelectThreads) {
+        const int v4 = base + lane;
+        const bool ok = v4 < nvec;
+        float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ok) q = __ldg(reinterpret_cast<const float4*>(z) + v4);
+        fn(float_key(q.x), 4 * v4 + 0, ok);
+        fn(float_key(q.y), 4 * v4 + 1, ok);
+        fn(float_key(q.z), 4 * v4 + 2, ok);
+        fn(float_key(q.w), 4 * v4 + 3, ok);
+      }
+      if (warp == 0)
+        for (int j = 4 * nvec + lane; j - lane < V; j += 32) {
+          const bool ok = j < V;
+          fn(float_key(ok ? z[j] : 0.0f), j, ok);
+        }
+    };
+
+    // Exact radix select over the current source: on return `prefix` is the key of
+    // the need0-th largest and `need` the number of elements equal to it to take.
+    uint32_t prefix = 0;   // key bits fixed so far
+    uint32_t need = K;     // elements still to take at or below the prefix
+    int fixed = 0;         // number of fixed high bits
+    auto radix_select = [&](uint32_t need0, bool may_shortcut) {
+    prefix = 0;
+    need = need0;
+    fixed = 0;
+    for (int level = 0; level < 3; ++level) {
+      const int bits = level < 2 ? 11 : 10;
+      const int shift = 32 - fixed - bits;
+      for (int b = tid; b < kSelectBins; b += kSelectThreads) hist[b] = 0;
+      __syncthreads();
+      for_each([&](uint32_t k, int, bool ok) {
+        const bool match = ok && (fixed == 0 || (k >> (32 - fixed)) == prefix);
+        hist_add(hist, (k >> shift) & ((1u << bits) - 1u), match);
+      });
+      __syncthreads();
+      // find the bin holding the need-th largest: thread t owns bins 4t .. 4t+3
+      const int nb = 1 << bits;
+      uint32_t mine = 0;
+      if (4 * tid < nb)
+        mine = hist[4 * tid] + hist[4 * tid + 1] + hist[4 * tid + 2] + hist[4 * tid + 3];
+      uint32_t incl = mine;  // suffix sum over this warp's lanes (higher lane = higher bins)
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      if (lane == 0) warp_sum[warp] = incl;
+      __syncthreads();
+      uint32_t above_warp = 0;
+      for (int w = warp + 1; w < kSelectWarps; ++w) above_warp += warp_sum[w];
+      const uint32_t above = above_warp + (incl - mine);  // bins owned by higher threads
+      if (4 * tid < nb && above < need && need <= above + mine) {
+        uint32_t acc = above;
+        for (int b = 4 * tid + 3; b >= 4 * tid; --b) {
+          if (acc + hist[b] >= need) {
+            s_bin = static_cast<uint32_t>(b);
+            s_above = acc;
+            break;
+          }
+          acc += hist[b];
+        }
+      }
+      __syncthreads();
+      const uint32_t bin = s_bin, above_bin = s_above;
+      const uint32_t in_bin = hist[bin];
+      __syncthreads();
+      if (may_shortcut && level == 0 && above_bin + in_bin <= static_cast<uint32_t>(kSelectCand)) {
+        // everything at or above the chosen top bin fits in shared memory: keep it
+        if (tid == 0) n_cand = 0;
+        __syncthreads();
+        for_each([&](uint32_t k, int id, bool ok) {
+          if (ok && (k >> shift) >= bin) {
+            const uint32_t slot = atomicAdd(&n_cand, 1u);
+            cand_key[slot] = k;
+            cand_idx[slot] = id;
+          }
+        });
+        __syncthreads();
+        in_smem = true;
+      }
+      prefix = (prefix << bits) | bin;
+      need -= above_bin;
+      fixed += bits;
+    }
+    };
+
+    // 1. threshold from a sample: every kSampleStride-th logit, selected in shared memory
+    const int stride = max(kSampleStride, (V + kSelectCand - 1) / kSelectCand);  // S <= kSelectCand
+    const int S = (V + stride - 1) / stride;
+    const uint32_t r = min(static_cast<uint32_t>(S),
+                           static_cast<uint32_t>((static_cast<int64_t>(K) * S + V - 1) / V) + 8u);
+    for (int i = tid; i < S; i += kSelectThreads) {
+      cand_key[i] = float_key(__ldg(z + static_cast<int64_t>(i) * stride));
+      cand_idx[i] = i * stride;
+    }
+    if (tid == 0) n_cand = static_cast<uint32_t>(S);
+    __syncthreads();
+    in_smem = true;
+    radix_select(r, false);
+    const uint32_t tau0 = prefix;
+    __syncthreads();
+    // 2. one pass over the row keeps every logit at or above tau0
+    if (tid == 0) n_cand = 0;
+    __syncthreads();
+    in_smem = false;
+    for_each([&](uint32_t k, int id, bool ok) {
+      if (ok && k >= tau0) {
+        const uint32_t slot = atomicAdd(&n_cand, 1u);
+        if (slot < static_cast<uint32_t>(kSelectCand)) {
+          cand_key[slot] = k;
+          cand_idx[slot] = id;
+        }
+      }
+    });
+    __syncthreads();
+    const uint32_t kept = n_cand;
+    __syncthreads();
+    if (kept >= static_cast<uint32_t>(K) && kept <= static_cast<uint32_t>(kSelectCand)) {
+      in_smem = true;          // the top K are among the kept logits
+      radix_select(K, false);
+    } else {
+      radix_select(K, true);   // select from the row itself
+    }
+    // prefix is now the exact key of the K-th largest; K - need keys are above it
+    const uint32_t tau = prefix;
+    const uint32_t n_above = static_cast<uint32_t>(K) - need;
+    if (tid == 0) {
+      n_gt = 0;
+      n_eq = 0;
+    }
+    __syncthreads();
+    for_each([&](uint32_t k, int id, bool ok) {
+      if (!ok) return;
+      if (k > tau) {
+        const uint32_t slot = atomicAdd(&n_gt, 1u);
+        ckey[slot] = k;
+        cidx[slot] = id;
+      } else if (k == tau) {
+        const uint32_t e = atomicAdd(&n_eq, 1u);
+        if (e < need) {
+          ckey[n_above + e] = k;
+          cidx[n_above + e] = id;
+        }
+      }
+    });
+    __syncthreads();
+    // bitonic sort of the K entries (padded to a power of two) by (key desc, id asc)
+    int P = 1;
+    while (P < K) P <<= 1;
+    for (int i = K + tid; i < P; i += kSelectThreads) {
+      ckey[i] = 0u;
+      cidx[i] = 0x7FFFFFFF;
+    }
+    __syncthreads();
+    for (int size = 2; size <= P; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < P; i += kSelectThreads) {
+          const int partner = i ^ stride;
+          if (partner > i) {
+            const bool desc = (i & size) == 0;  // blocks alternate; the final pass is descending
+            const uint32_t ka = ckey[i], kb = ckey[partner];
+            const int ia = cidx[i], ib = cidx[partner];
+            // "a before b" in the final order: larger key, then smaller id
+            const bool a_first = (ka > kb) || (ka == kb && ia < ib);
+            if (a_first != desc) {
+              ckey[i] = kb;
+              ckey[partner] = ka;
+              cidx[i] = ib;
+              cidx[partner] = ia;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = tid; i < K; i += kSelectThreads) {
+      out_idx[row * K + i] = cidx[i];
+      out_val[row * K + i] = key_float(ckey[i]);
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace kd
