@@ -30,6 +30,9 @@ constexpr int kSelectBins = 2048;
 constexpr int kSelectMaxK = 256;
 constexpr int kSelectCand = 3072;  // candidates kept in shared memory
 constexpr int kSampleStride = 64;  // the threshold sample takes at most every 64th logit
+// The bin search gives each thread four consecutive bins: all bins must be owned.
+static_assert(4 * kSelectThreads >= kSelectBins, "every histogram bin needs an owning thread");
+static_assert(kSelectThreads >= 32 * kSelectWarps && kSelectMaxK <= kSelectCand, "select shape");
 
 // Larger float -> larger key (sign flipped for positives, all bits for negatives).
 __device__ __forceinline__ uint32_t float_key(float v) {
