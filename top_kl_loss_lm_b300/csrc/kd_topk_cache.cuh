@@ -114,6 +114,10 @@ __global__ void __launch_bounds__(kSelectThreads)
       const int bits = level < 2 ? 11 : 10;
       const int shift = 32 - fixed - bits;
       for (int b = tid; b < kSelectBins; b += kSelectThreads) hist[b] = 0;
+      if (tid == 0) {  // always a valid bin, even if no thread were to claim one
+        s_bin = 0;
+        s_above = 0;
+      }
       __syncthreads();
       for_each([&](uint32_t k, int, bool ok) {
         const bool match = ok && (fixed == 0 || (k >> (32 - fixed)) == prefix);
