@@ -64,7 +64,7 @@ def traffic_file(workload: str) -> str:
     return os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.json")
 KERNEL_SOURCES = ("kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h", "kd_logits.cuh", "kd_topk_cache.cuh")
 # template argument of kd_gemm_kernel -> category of the library's launch timing
-GEMM_EPI = {"0": "fwd_gemm", "1": "dz_gemm", "2": "dh_gemm", "3": "dw_gemm"}
+GEMM_EPI = {"0": "fwd_gemm", "1": "dz_gemm", "2": "dh_gemm", "3": "dw_gemm", "4": "topk_gemm"}
 
 
 def kernel_source_hash() -> str:
@@ -92,8 +92,9 @@ def traffic_from_ncu_csv(csv_path: str, workload: str, chunk: int) -> dict:
                 continue
             d = dict(zip(hdr, r))
             m = re.search(r"kd_gemm_kernel<(\d)", d["Kernel Name"])
-            cat = GEMM_EPI[m.group(1)] if m else ("logits" if "kd_logits_kernel" in d["Kernel Name"]
-                                                  else None)
+            name = d["Kernel Name"]
+            cat = (GEMM_EPI[m.group(1)] if m else "logits" if "kd_logits_kernel" in name
+                   else "topk_select" if "kd_topk_select_kernel" in name else None)
             if cat is None or d["Metric Name"] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
                 continue
             unit = d.get("Metric Unit", "byte").lower()
@@ -750,7 +751,8 @@ def run_sweep(args):
 def main():
     args = parse()
     if args.traffic_from:
-        name, chunk = ("gptoss_logits", 0) if args.logits else (args.workload, args.chunk)
+        name, chunk = (("gptoss_logits", 0) if args.logits else ("gptoss_teacher", 0)
+                       if args.teacher_topk else (args.workload, args.chunk))
         rec = traffic_from_ncu_csv(args.traffic_from, name, chunk)
         with open(traffic_file(name), "w") as f:
             json.dump(rec, f, indent=1)
