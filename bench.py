@@ -68,11 +68,17 @@ GEMM_EPI = {"0": "fwd_gemm", "1": "dz_gemm", "2": "dh_gemm", "3": "dw_gemm", "4"
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code: comments and runs of whitespace are
+    dropped first, so a record stays valid across comment-only edits."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "top_kl_loss_lm_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "top_kl_loss_lm_b300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -63,11 +63,12 @@ typedef struct CUstream_st* kd_stream_t;
 
 /*
  * Bytes of device workspace that kd_topk_kl_fwd and kd_topk_kl_bwd need for
- * these sizes (one buffer serves both calls). The only vocabulary-sized part
- * is one chunk of dZ (chunk_tokens x V bf16), so the size grows linearly in N
- * and never as N x V. chunk_tokens is the backward's row-chunk C (rounded up
- * to a multiple of 128 internally; <= 0 selects 4096). Returns 0 for invalid
- * sizes. Pure host arithmetic; safe without a GPU.
+ * these sizes (one buffer serves both calls). The only vocabulary-sized parts
+ * are two chunks of dZ (chunk_tokens x V bf16 each; one when N fits in one
+ * chunk), so the size grows linearly in N and never as N x V. chunk_tokens is
+ * the backward's row-chunk C (rounded up to a multiple of 256 internally; <= 0
+ * selects 4096). Returns 0 for invalid sizes. Pure host arithmetic; safe
+ * without a GPU.
  */
 size_t kd_topk_kl_workspace_size(int64_t N, int D, int V, int K, int64_t chunk_tokens);
 

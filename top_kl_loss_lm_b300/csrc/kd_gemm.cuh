@@ -1,11 +1,17 @@
 // kd_gemm.cuh — persistent, warp-specialised tcgen05 GEMM for sm_103a with the
 // loss epilogues fused in.
 //
-//   warp 0      TMA producer: fills a STAGES-deep ring of (A, B) k-blocks
-//   warp 1      TMEM owner + MMA issuer: 128 x BN x 16 bf16 MMAs into one of two
-//               fp32 TMEM accumulators (2 x 256 columns), so the epilogue of one
-//               tile overlaps the main loop of the next
-//   warps 2..5  epilogue: each thread owns one accumulator row (TMEM lane)
+// The loss runs it on CTA pairs (cluster of 2, cta_group::2): a 256 x BN tile per
+// pair, each CTA holding 128 rows of A and half of B per k-block; the single-CTA
+// form (128 x BN tiles) remains for the GEMM test hook.
+//
+//   warp 0      TMA producer: fills a STAGES-deep ring of (A, B) k-blocks (on a
+//               pair, both CTAs' copies complete on the first CTA's barrier)
+//   warp 1      TMEM owner + MMA issuer (first CTA of a pair): M x BN x 16 bf16
+//               MMAs into one of two fp32 TMEM accumulators (2 x 256 columns),
+//               so the epilogue of one tile overlaps the main loop of the next
+//   warps 2..5  epilogue: each thread owns one accumulator row (TMEM lane) of
+//               its CTA
 //
 // Epilogues:
 //   kEpiFwd   online max / sum-of-exp of Z/T over the unit's vocabulary tiles

@@ -2,11 +2,14 @@
 // descriptors, and the launch sequence of the forward and backward.
 //
 // Forward  (one pass over the vocabulary, nothing tokens x vocabulary stored):
-//   prep -> fused GEMM + online logsumexp + top-K gather -> combine
+//   prep -> per 4,096 rows: fused GEMM + online logsumexp + top-K gather -> combine
 // Backward (the logits are recomputed, C tokens at a time):
-//   prep -> for each chunk: GEMM + dZ epilogue (dZ chunk, bf16)
-//                           -> dH = dZ W  (split over V, fixed-order sum)
-//                           -> dW (+)= dZ^T H
+//   prep -> for each group of kDwGroup chunks:
+//             for each chunk: GEMM + dZ epilogue (the chunk's dZ slot, bf16)
+//                             -> dH = dZ W  (split over V, fixed-order sum)
+//             dW (+)= dZ^T H over the group's tokens
+// Also: the loss from materialised logits (kd_topk_kl_logits) and the teacher's
+// top-K cache (kd_teacher_topk: logit GEMM per chunk + exact per-row selection).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
