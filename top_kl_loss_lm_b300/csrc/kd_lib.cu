@@ -715,6 +715,23 @@ int64_t topk_chunk_rows(int64_t N) {
   return N < c ? cdiv(N < 1 ? 1 : N, kTileRows) * kTileRows : c;
 }
 inline int64_t topk_ld(int V) { return cdiv(V, 8) * 8; }
+
+// Resident select CTAs per SM, with the carveout set to favour shared memory (the
+// kernel's 35 KB of shared arrays would otherwise limit an SM to three CTAs).
+int select_blocks_per_sm() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(kd_topk_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kd_topk_select_kernel, kSelectThreads, 0) !=
+            cudaSuccess ||
+        n < 1)
+      n = 1;
+    cudaGetLastError();
+  });
+  return n;
+}
 }  // namespace
 }  // namespace kd
 
@@ -763,7 +780,8 @@ extern "C" kd_status kd_teacher_topk(const uint16_t* H, const uint16_t* W, int64
       if ((st = launch_gemm<kEpiPlain, false, false, kPair>(mH, mW, mZ, a, di, s)) != KD_OK)
         return st;
     }
-    int64_t grid = 4L * di->num_sms;
+    // persistent: as many CTAs as are resident at once (each CTA loops over rows)
+    int64_t grid = static_cast<int64_t>(select_blocks_per_sm()) * di->num_sms;
     if (grid > rows) grid = rows;
     ProfScope ps(kProfTopkSelect, s);
     kd_topk_select_kernel<<<static_cast<unsigned>(grid), kSelectThreads, 0, s>>>(

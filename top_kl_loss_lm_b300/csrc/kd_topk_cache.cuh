@@ -10,9 +10,10 @@
 // equal to it as are still needed, and a bitonic sort orders the K of them
 // (descending logit, then ascending id).
 //
-// The row is normally read once. A strided sample of the row (every 64th logit,
-// or sparser so that it fits in shared memory) is selected first, in shared
-// memory, to a key tau0 that about K + 8 sample strides' worth of logits exceed; one pass over the row copies every logit at or above tau0
+// The row is normally read once. A sample of the row (runs of 8 consecutive
+// logits, one logit in 64 or fewer so that it fits in shared memory) is selected
+// first, in shared memory, to a key tau0 that about K + 8 sample strides' worth
+// of logits exceed; one pass over the row copies every logit at or above tau0
 // (a few hundred) to shared memory, and the exact radix select and the sort
 // then run there. If that set holds fewer than K logits or more than
 // kSelectCand (heavily tied logits), the row is selected directly: the first
@@ -84,15 +85,25 @@ __global__ void __launch_bounds__(kSelectThreads)
         }
         return;
       }
-      for (int base = warp * 32; base < nvec; base += kSelectThreads) {
-        const int v4 = base + lane;
-        const bool ok = v4 < nvec;
-        float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ok) q = __ldg(reinterpret_cast<const float4*>(z) + v4);
-        fn(float_key(q.x), 4 * v4 + 0, ok);
-        fn(float_key(q.y), 4 * v4 + 1, ok);
-        fn(float_key(q.z), 4 * v4 + 2, ok);
-        fn(float_key(q.w), 4 * v4 + 3, ok);
+      // four 16-byte loads in flight per thread before any of them is used
+      constexpr int kUnroll = 4;
+      for (int base = warp * 32; base < nvec; base += kUnroll * kSelectThreads) {
+        float4 q[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v4 = base + u * kSelectThreads + lane;
+          q[u] = v4 < nvec ? __ldg(reinterpret_cast<const float4*>(z) + v4)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v4 = base + u * kSelectThreads + lane;
+          const bool ok = v4 < nvec;
+          fn(float_key(q[u].x), 4 * v4 + 0, ok);
+          fn(float_key(q[u].y), 4 * v4 + 1, ok);
+          fn(float_key(q[u].z), 4 * v4 + 2, ok);
+          fn(float_key(q[u].w), 4 * v4 + 3, ok);
+        }
       }
       if (warp == 0)
         for (int j = 4 * nvec + lane; j - lane < V; j += 32) {
@@ -176,13 +187,17 @@ __global__ void __launch_bounds__(kSelectThreads)
     };
 
     // 1. threshold from a sample: every kSampleStride-th logit, selected in shared memory
-    const int stride = max(kSampleStride, (V + kSelectCand - 1) / kSelectCand);  // S <= kSelectCand
-    const int S = (V + stride - 1) / stride;
+    // the sample is runs of 8 consecutive logits (one 32-byte sector each), one run
+    // every 8 * stride logits; positions past V get the smallest key
+    const int stride = max(kSampleStride, (V + kSelectCand - 1) / kSelectCand);
+    const int runs = (V + 8 * stride - 1) / (8 * stride);
+    const int S = 8 * runs;  // <= kSelectCand
     const uint32_t r = min(static_cast<uint32_t>(S),
                            static_cast<uint32_t>((static_cast<int64_t>(K) * S + V - 1) / V) + 8u);
     for (int i = tid; i < S; i += kSelectThreads) {
-      cand_key[i] = float_key(__ldg(z + static_cast<int64_t>(i) * stride));
-      cand_idx[i] = i * stride;
+      const int j = (i >> 3) * (8 * stride) + (i & 7);
+      cand_key[i] = j < V ? float_key(__ldg(z + j)) : 0u;
+      cand_idx[i] = j;
     }
     if (tid == 0) n_cand = static_cast<uint32_t>(S);
     __syncthreads();
