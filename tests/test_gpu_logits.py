@@ -83,10 +83,12 @@ def test_gradient_in_place_and_loss_only():
     ref = _run(p, Z)
     inplace = _run(p, Z, in_place=True)
     assert torch.equal(ref["dZ"], inplace["dZ"])
-    only = _run(p, Z, grad=False)
+    only = _run(p, Z, grad=False)  # a different kernel shape: same values up to fp32 order
     assert only["status"] == 0
-    assert torch.equal(only["loss"], ref["loss"]) and torch.equal(only["lse"], ref["lse"])
+    assert torch.allclose(only["loss"], ref["loss"], rtol=1e-5, atol=1e-6)
+    assert torch.allclose(only["lse"], ref["lse"], rtol=1e-6, atol=1e-6)
     _compare(p, Z, ref)
+    _compare(p, Z, only)
 
 
 def test_k_extremes_duplicates_and_empty():
@@ -113,6 +115,13 @@ def test_strided_rows_and_argument_errors():
     _compare(p, Z, out)
     with pytest.raises(binding.KdError):  # V not a multiple of 8
         _run(p, Zbig[:, :1020])
+
+
+@pytest.mark.parametrize("V", [4096, 201088])
+def test_loss_only_shapes(V):
+    # without the gradient the library runs lighter CTAs, four per SM, one row buffer
+    p, Z = _logits_problem(700, V, 256, 1.3, seed=17, mask="frac", mask_frac=0.05)
+    _compare(p, Z, _run(p, Z, grad=False))
 
 
 @pytest.mark.slow

@@ -107,6 +107,17 @@ def test_accumulate_dw():
     P.assert_grad_close((gpu["dW"] - init).double().cpu().numpy(), ref["dW"], "dW accumulated")
 
 
+def test_accumulate_dw_over_several_dw_groups():
+    # 1,000 rows in 256-row chunks: dW is contracted over two chunks per launch,
+    # so this runs two groups (the second ending in a short chunk) and adds onto dW_init
+    p = make_problem(1000, 72, 1300, 8, 1.4, seed=16, mask="frac", mask_frac=0.05, device=DEV)
+    init = torch.randn(p.V, p.D, device=DEV) * 1e-3
+    gpu = P.run_gpu(p, chunk_tokens=256, accumulate=True, dW_init=init)
+    ref = P.run_oracle(p, gpu["g"].double().cpu().numpy())
+    P.assert_grad_close(gpu["dH"].double().cpu().numpy(), ref["dH"], "dH")
+    P.assert_grad_close((gpu["dW"] - init).double().cpu().numpy(), ref["dW"], "dW accumulated")
+
+
 def test_invalid_id_at_counted_row_is_reported():
     p = make_problem(64, 64, 300, 4, 1.0, seed=12, mask="frac", mask_frac=0.25, device=DEV)
     masked = torch.nonzero(p.mask == 0)[0, 0].item()

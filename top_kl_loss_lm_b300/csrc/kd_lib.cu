@@ -574,25 +574,31 @@ inline int logits_slice(int V, int cl) { return static_cast<int>(cdiv(cdiv(V, cl
 
 constexpr size_t kLogitsSmemLimit = 227 * 1024;
 
-// Cluster size: the smallest whose slices, two row buffers each, let two CTAs
-// share an SM (two independent row pipelines per SM keep enough bytes in
-// flight: 78% of the HBM copy bandwidth at V = 201,088 against 67% with one
-// CTA per SM and 49% with a four-buffer ring), else the smallest that fits one
-// CTA per SM. Returns false if no cluster size fits.
-bool logits_shape(int V, int* cl_out, int* nbuf_out) {
-  *nbuf_out = 2;
-  for (int per_sm = 2; per_sm >= 1; --per_sm)
+// Shape of the loss-from-logits kernel. With the gradient: the smallest cluster
+// whose slices, two row buffers each, let two CTAs of 256 compute threads share
+// an SM (two independent row pipelines per SM keep enough bytes in flight: 78%
+// of the HBM copy bandwidth at V = 201,088 against 67% with one CTA per SM and
+// 49% with a four-buffer ring), else the smallest that fits one CTA per SM.
+// Loss only: one row buffer and 128 compute threads per CTA, four CTAs per SM
+// (80% against 65% with the gradient's shape). Returns false if nothing fits.
+struct LogitsShape {
+  int cl, nbuf, threads;
+};
+bool logits_shape(int V, bool grad, LogitsShape* out) {
+  const int nbuf = grad ? 2 : 1;
+  const int threads = grad ? kLogitsThreads : kLogitsThreadsLossOnly;
+  for (int per_sm = grad ? 2 : 4; per_sm >= 1; per_sm = per_sm > 2 ? 2 : per_sm - 1)
     for (int cl = 1; cl <= kLogitsMaxCluster; cl *= 2)
-      if (per_sm * logits_smem_bytes(logits_slice(V, cl), 2) <= kLogitsSmemLimit) {
-        *cl_out = cl;
+      if (per_sm * logits_smem_bytes(logits_slice(V, cl), nbuf) <= kLogitsSmemLimit) {
+        *out = {cl, nbuf, threads};
         return true;
       }
   return false;
 }
 
-template <int CL, int NBUF>
+template <int CL, int NBUF, int NT>
 kd_status launch_logits(const LogitsArgs& a, const DevInfo* di, cudaStream_t s) {
-  auto kern = kd_logits_kernel<CL, NBUF>;
+  auto kern = kd_logits_kernel<CL, NBUF, NT>;
   const size_t smem = logits_smem_bytes(a.Vs, NBUF);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess) {
@@ -606,7 +612,7 @@ kd_status launch_logits(const LogitsArgs& a, const DevInfo* di, cudaStream_t s) 
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(di->num_sms / CL * CL));
-  cfg.blockDim = dim3(kLogitsBlock);
+  cfg.blockDim = dim3(NT + 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -655,8 +661,8 @@ extern "C" kd_status kd_topk_kl_logits(const uint16_t* Z, int64_t ldz, const int
       !aligned(topk_logit, 4) || !aligned(loss, 4) || !aligned(lse, 4) || !aligned(n_valid, 8) ||
       (dloss && !aligned(dloss, 4)))
     return KD_ERR_ALIGN;
-  int cl = 0, nbuf = 0;
-  if (!logits_shape(V, &cl, &nbuf)) return KD_ERR_UNSUPPORTED;
+  LogitsShape shape;
+  if (!logits_shape(V, dZ != nullptr, &shape)) return KD_ERR_UNSUPPORTED;
   kd_status st = KD_OK;
   const DevInfo* di = device_info(&st);
   if (!di) return st;
@@ -690,18 +696,25 @@ extern "C" kd_status kd_topk_kl_logits(const uint16_t* Z, int64_t ldz, const int
   a.N = N;
   a.V = V;
   a.K = K;
-  a.Vs = logits_slice(V, cl);
+  a.Vs = logits_slice(V, shape.cl);
   a.scale2 = 1.4426950408889634f * inv_T;
   a.inv_T = inv_T;
   a.status = di->status;
   a.timeout_ns = 2000000000ull;
   ProfScope ps(kProfLogits, s);
-  if (nbuf != 2) return KD_ERR_UNSUPPORTED;
-  switch (cl) {
-    case 1: return launch_logits<1, 2>(a, di, s);
-    case 2: return launch_logits<2, 2>(a, di, s);
-    case 4: return launch_logits<4, 2>(a, di, s);
-    default: return launch_logits<8, 2>(a, di, s);
+  if (shape.nbuf == 2 && shape.threads == kLogitsThreads) {  // with the gradient
+    switch (shape.cl) {
+      case 1: return launch_logits<1, 2, kLogitsThreads>(a, di, s);
+      case 2: return launch_logits<2, 2, kLogitsThreads>(a, di, s);
+      case 4: return launch_logits<4, 2, kLogitsThreads>(a, di, s);
+      default: return launch_logits<8, 2, kLogitsThreads>(a, di, s);
+    }
+  }
+  switch (shape.cl) {  // loss only
+    case 1: return launch_logits<1, 1, kLogitsThreadsLossOnly>(a, di, s);
+    case 2: return launch_logits<2, 1, kLogitsThreadsLossOnly>(a, di, s);
+    case 4: return launch_logits<4, 1, kLogitsThreadsLossOnly>(a, di, s);
+    default: return launch_logits<8, 1, kLogitsThreadsLossOnly>(a, di, s);
   }
 }
 

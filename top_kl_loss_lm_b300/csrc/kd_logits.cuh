@@ -35,9 +35,9 @@
 
 namespace kd {
 
-constexpr int kLogitsThreads = 256;  // compute threads (warps 1..8); warp 0 drives the copies
-constexpr int kLogitsWarps = kLogitsThreads / 32;
-constexpr int kLogitsBlock = kLogitsThreads + 32;
+constexpr int kLogitsThreads = 256;  // compute threads (warps 1..8) with the gradient
+constexpr int kLogitsThreadsLossOnly = 128;  // loss only: lighter CTAs, four per SM
+constexpr int kLogitsMaxWarps = kLogitsThreads / 32;
 constexpr int kLogitsMaxCluster = 8;
 constexpr int kLogitsMaxBuffers = 4;
 
@@ -64,7 +64,7 @@ struct LogitsArgs {
 __host__ __device__ constexpr size_t logits_smem_bytes(int Vs, int nbuf) {
   return static_cast<size_t>(nbuf) * Vs * 2      // row slices (bf16)
          + 2 * kLogitsMaxCluster * 16            // cluster partials, two parities
-         + 2 * kLogitsWarps * 16                 // block reduction scratch, two parities
+         + 2 * kLogitsMaxWarps * 16              // block reduction scratch, two parities
          + (2 * kLogitsMaxBuffers + 2) * 8 + 16; // full / empty / exchange barriers, abort flag
 }
 
@@ -82,19 +82,22 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Barrier among the compute warps only (named barrier 1).
+// Barrier among the NT compute threads only (named barrier 1).
+template <int NT>
 __device__ __forceinline__ void compute_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kLogitsThreads) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
-template <int CL, int NBUF>
-__global__ void __launch_bounds__(kLogitsBlock, 2) kd_logits_kernel(const LogitsArgs a) {
+// CL: CTAs per row (cluster size); NBUF: row buffers per CTA; NT: compute threads.
+template <int CL, int NBUF, int NT>
+__global__ void __launch_bounds__(NT + 32, NT <= 128 ? 4 : 2) kd_logits_kernel(const LogitsArgs a) {
+  constexpr int kLogitsWarps = NT / 32;
   extern __shared__ __align__(128) uint8_t smem[];
   const size_t slice_bytes = static_cast<size_t>(a.Vs) * 2;
   auto buf = [&](int b) { return reinterpret_cast<uint16_t*>(smem + b * slice_bytes); };
   float4* exch = reinterpret_cast<float4*>(smem + NBUF * slice_bytes);  // [2][kLogitsMaxCluster]
-  float4* red = exch + 2 * kLogitsMaxCluster;                          // [2][warps]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kLogitsWarps);
+  float4* red = exch + 2 * kLogitsMaxCluster;                          // [2][max warps]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kLogitsMaxWarps);
   uint64_t* empty = full + kLogitsMaxBuffers;
   uint64_t* xbar = empty + kLogitsMaxBuffers;                          // [2]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(xbar + 2);
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(kLogitsBlock, 2) kd_logits_kernel(const Logits
       float zk = 0.0f;
       bool mine = false;  // this thread's teacher entry falls in the slice
       if (work) {
-        for (int v = ctid; v < nvec; v += kLogitsThreads) {
+        for (int v = ctid; v < nvec; v += NT) {
           const uint4 w = *reinterpret_cast<const uint4*>(zrow + 8 * v);
           const float z[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                               bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
@@ -194,12 +197,18 @@ __global__ void __launch_bounds__(kLogitsBlock, 2) kd_logits_kernel(const Logits
           ms.y = ms.y * ex2_approx(ms.x - mnew) + s;
           ms.x = mnew;
         }
-        if (ctid < K) {
-          pr = __ldg(&a.pairs[row * K + ctid]);
-          if (pr.x >= lo && pr.x < lo + len) {
-            zk = __uint_as_float(static_cast<uint32_t>(zrow[pr.x - lo]) << 16);
-            cross = __int_as_float(pr.y) * zk;
-            mine = true;
+        // teacher entries ctid, ctid + NT, ...; the first one is kept for the
+        // gradient's correction (with the gradient NT >= K, so that is every entry)
+        for (int k = ctid; k < K; k += NT) {
+          const int2 q = __ldg(&a.pairs[row * K + k]);
+          if (q.x >= lo && q.x < lo + len) {
+            const float zq = __uint_as_float(static_cast<uint32_t>(zrow[q.x - lo]) << 16);
+            cross += __int_as_float(q.y) * zq;
+            if (k == ctid) {
+              pr = q;
+              zk = zq;
+              mine = true;
+            }
           }
         }
       }
@@ -212,7 +221,7 @@ __global__ void __launch_bounds__(kLogitsBlock, 2) kd_logits_kernel(const Logits
       }
       float4* rd = red + par * kLogitsWarps;
       if (lane == 0) rd[cwarp] = make_float4(ms.x, ms.y, cross, 0.0f);
-      compute_sync();
+      compute_sync<NT>();
       float2 rms = make_float2(-INFINITY, 0.0f);
       float rcross = 0.0f;
 #pragma unroll
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(kLogitsBlock, 2) kd_logits_kernel(const Logits
       if (grad && work) {
         const float gs = counted ? a.dloss[row] * a.inv_T : 0.0f;
         uint16_t* drow = buf(b);
-        for (int v = ctid; v < nvec; v += kLogitsThreads) {
+        for (int v = ctid; v < nvec; v += NT) {
           uint4* p = reinterpret_cast<uint4*>(drow + 8 * v);
           uint4 w = *p;
           if (counted) {
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(kLogitsBlock, 2) kd_logits_kernel(const Logits
           }
           *p = w;
         }
-        compute_sync();  // the vectors are written before single entries are corrected
+        compute_sync<NT>();  // the vectors are written before single entries are corrected
         if (counted && mine && (ctid == 0 || __ldg(&a.pairs[row * K + ctid - 1]).x != pr.x)) {
           float P = __int_as_float(pr.y);  // merge a run of repeated ids
           for (int k2 = ctid + 1; k2 < K; ++k2) {
