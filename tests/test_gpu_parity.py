@@ -50,7 +50,7 @@ def test_forward_row_chunks_with_ragged_tail():
     _full(p, chunk=1536)
 
 
-@pytest.mark.parametrize("T", [0.7, 2.0])
+@pytest.mark.parametrize("T", [0.1, 0.7, 2.0])
 def test_teacher_covers_vocabulary(T):
     p = make_problem(64, 64, 200, 200, T, seed=3, device=DEV)
     _full(p)
