@@ -64,6 +64,7 @@ struct Geo {
   static constexpr int kSmemBytes = kRingBytes + kStagingBytes + 1024 /*align*/ + 256 /*barriers*/;
 };
 constexpr int kSlabBytes = 64 * kBK * 2;         // one 64-wide MN slab of a k-block: 8 KB
+constexpr int kFwdExtraStages = 1;               // ring stages the forward gains from staging
 constexpr int kGemmThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kGemmSmemBytes = Geo<false>::kSmemBytes > Geo<true>::kSmemBytes ? Geo<false>::kSmemBytes
@@ -197,10 +198,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* staging = smem + G::kRingBytes;  // 1024-byte aligned
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + kStagingBytes);
-  uint64_t* empty_bar = full_bar + G::kStages;
-  uint64_t* acc_full = empty_bar + G::kStages;
+  // The forward's epilogue sends nothing through shared memory, so on a CTA pair
+  // its staging area becomes one more ring stage (same total shared memory).
+  constexpr bool kStaging = EPI != kEpiFwd || !PAIR;
+  constexpr int kStages = kStaging ? G::kStages : G::kStages + kFwdExtraStages;
+  static_assert(kStaging || kFwdExtraStages * G::kStageBytes <= kStagingBytes, "ring fits");
+  uint8_t* staging = smem + kStages * G::kStageBytes;  // 1024-byte aligned
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + (kStaging ? kStagingBytes : 0));
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* acc_full = empty_bar + kStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain_bar = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int64_t unit_step = PAIR ? (gridDim.x >> 1) : gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < G::kStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                               k0 + args.b_k_off);
               }
             }
-            if (++stage == G::kStages) {
+            if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
@@ -353,7 +359,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             any_mma = true;
             umma_commit<PAIR>(&empty_bar[stage]);
-            if (++stage == G::kStages) {
+            if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
