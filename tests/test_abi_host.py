@@ -128,3 +128,13 @@ def test_dh_split_fills_the_last_wave(lib):
     units = info["units"]
     assert info["k_splits"] > 1
     assert units / (-(-units // 74) * 74) > 0.95
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no CPU or library fallback: without libkdtopk.so every call raises
+    monkeypatch.setattr(binding, "_LIB", None)
+    monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "libkdtopk.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.kd_topk_kl_workspace_size(16, 8, 32, 2)
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.lib()
