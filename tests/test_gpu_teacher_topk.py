@@ -7,7 +7,8 @@ ids valid and distinct, logits in descending order, each returned logit equal
 to the exact logit of its id within the fp32 accumulation error, no id left out
 whose exact logit beats the smallest returned one by more than that error, and
 the returned values equal the oracle's top-K values within it. Ties are
-exercised on purpose (repeated rows of W, an all-zero hidden state).
+exercised on purpose (repeated rows of W, an all-zero hidden state); tied
+logits go to the smallest ids, so repeated calls return the same cache.
 """
 import numpy as np
 import pytest
@@ -82,6 +83,10 @@ def test_ties_and_all_equal_row(V):
     ids, vals = _run(H, W, 32)
     _check(H, W, 32, ids, vals)
     assert np.all(vals[5] == 0)
+    # ties go to the smallest ids, so the cache is the same on every call
+    assert list(ids[5]) == list(range(32))
+    ids2, vals2 = _run(H, W, 32)
+    assert np.array_equal(ids, ids2) and np.array_equal(vals, vals2)
 
 
 def test_several_row_chunks():

@@ -6,9 +6,10 @@
 // found exactly by a three-level radix select on an order-preserving 32-bit key
 // (11, 11 and 10 bits): each level histograms, in shared memory, the keys whose
 // higher bits match the prefix found so far and picks the bin that holds the
-// K-th largest. A last pass collects every element above that key and as many
-// equal to it as are still needed, and a bitonic sort orders the K of them
-// (descending logit, then ascending id).
+// K-th largest. A last pass collects every element above that key and, of those
+// equal to it, the ones with the smallest ids (a radix select on the ids when
+// more are tied than needed), and a bitonic sort orders the K of them
+// (descending logit, then ascending id): the result is deterministic.
 //
 // The row is normally read once. A sample of the row (runs of 8 consecutive
 // logits, one logit in 64 or fewer so that it fits in shared memory) is selected
@@ -53,7 +54,7 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool acti
   if ((__ffs(peers) - 1) == static_cast<int>(threadIdx.x & 31)) atomicAdd(&hist[bin], __popc(peers));
 }
 
-__global__ void __launch_bounds__(kSelectThreads)
+__global__ void __launch_bounds__(kSelectThreads, 3)
     kd_topk_select_kernel(const float* __restrict__ Z, int64_t ldz, int64_t rows, int V, int K,
                           int32_t* __restrict__ out_idx, float* __restrict__ out_val) {
   __shared__ uint32_t hist[kSelectBins];
@@ -113,11 +114,15 @@ __global__ void __launch_bounds__(kSelectThreads)
     };
 
     // Exact radix select over the current source: on return `prefix` is the key of
-    // the need0-th largest and `need` the number of elements equal to it to take.
+    // the need0-th largest, `need` the number of elements equal to it to take and
+    // eq_last how many elements carry that key. With by_id the keys are ~id of the
+    // elements whose logit key equals tau_sel, so the need0-th largest of them
+    // marks the need0-th smallest id among logits tied at tau_sel.
     uint32_t prefix = 0;   // key bits fixed so far
     uint32_t need = K;     // elements still to take at or below the prefix
+    uint32_t eq_last = 0;  // elements whose whole key equals the result
     int fixed = 0;         // number of fixed high bits
-    auto radix_select = [&](uint32_t need0, bool may_shortcut) {
+    auto radix_select = [&](uint32_t need0, bool may_shortcut, bool by_id, uint32_t tau_sel) {
     prefix = 0;
     need = need0;
     fixed = 0;
@@ -130,9 +135,11 @@ __global__ void __launch_bounds__(kSelectThreads)
         s_above = 0;
       }
       __syncthreads();
-      for_each([&](uint32_t k, int, bool ok) {
-        const bool match = ok && (fixed == 0 || (k >> (32 - fixed)) == prefix);
-        hist_add(hist, (k >> shift) & ((1u << bits) - 1u), match);
+      for_each([&](uint32_t k, int id, bool ok) {
+        const uint32_t key = by_id ? ~static_cast<uint32_t>(id) : k;
+        const bool match = ok && (!by_id || k == tau_sel) &&
+                           (fixed == 0 || (key >> (32 - fixed)) == prefix);
+        hist_add(hist, (key >> shift) & ((1u << bits) - 1u), match);
       });
       __syncthreads();
       // find the bin holding the need-th largest: thread t owns bins 4t .. 4t+3
@@ -166,7 +173,9 @@ __global__ void __launch_bounds__(kSelectThreads)
       const uint32_t bin = s_bin, above_bin = s_above;
       const uint32_t in_bin = hist[bin];
       __syncthreads();
-      if (may_shortcut && level == 0 && above_bin + in_bin <= static_cast<uint32_t>(kSelectCand)) {
+      if (level == 2) eq_last = in_bin;
+      if (may_shortcut && !by_id && level == 0 &&
+          above_bin + in_bin <= static_cast<uint32_t>(kSelectCand)) {
         // everything at or above the chosen top bin fits in shared memory: keep it
         if (tid == 0) n_cand = 0;
         __syncthreads();
@@ -202,7 +211,7 @@ __global__ void __launch_bounds__(kSelectThreads)
     if (tid == 0) n_cand = static_cast<uint32_t>(S);
     __syncthreads();
     in_smem = true;
-    radix_select(r, false);
+    radix_select(r, false, false, 0u);
     const uint32_t tau0 = prefix;
     __syncthreads();
     // 2. one pass over the row keeps every logit at or above tau0
@@ -223,13 +232,21 @@ __global__ void __launch_bounds__(kSelectThreads)
     __syncthreads();
     if (kept >= static_cast<uint32_t>(K) && kept <= static_cast<uint32_t>(kSelectCand)) {
       in_smem = true;          // the top K are among the kept logits
-      radix_select(K, false);
+      radix_select(K, false, false, 0u);
     } else {
-      radix_select(K, true);   // select from the row itself
+      radix_select(K, true, false, 0u);   // select from the row itself
     }
     // prefix is now the exact key of the K-th largest; K - need keys are above it
     const uint32_t tau = prefix;
-    const uint32_t n_above = static_cast<uint32_t>(K) - need;
+    const uint32_t take_eq = need;
+    const uint32_t n_above = static_cast<uint32_t>(K) - take_eq;
+    // more logits tied at tau than needed: take the ones with the smallest ids, so
+    // the result does not depend on thread timing
+    uint32_t id_cut = 0;  // take tied logits whose ~id >= id_cut
+    if (eq_last > take_eq) {
+      radix_select(take_eq, false, true, tau);
+      id_cut = prefix;
+    }
     if (tid == 0) {
       n_gt = 0;
       n_eq = 0;
@@ -241,9 +258,9 @@ __global__ void __launch_bounds__(kSelectThreads)
         const uint32_t slot = atomicAdd(&n_gt, 1u);
         ckey[slot] = k;
         cidx[slot] = id;
-      } else if (k == tau) {
+      } else if (k == tau && ~static_cast<uint32_t>(id) >= id_cut) {
         const uint32_t e = atomicAdd(&n_eq, 1u);
-        if (e < need) {
+        if (e < take_eq) {  // exactly take_eq qualify; the guard only bounds the slots
           ckey[n_above + e] = k;
           cidx[n_above + e] = id;
         }
