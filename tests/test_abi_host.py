@@ -100,6 +100,7 @@ SHAPES = [
     (1, 4096, 2880, 201088),    # dH of one 4096-token chunk
     (1, 300, 136, 1000),
     (2, 201088, 2880, 4096),    # dW of one chunk
+    (2, 201088, 2880, 8192),    # dW of a two-chunk group
     (2, 1000, 136, 300),
 ]
 
