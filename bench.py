@@ -728,6 +728,9 @@ def run_sweep(args):
 
     from workloads import make_problem
     for N in (4096, 16384, 65536, 131072, 262144):
+        torch.cuda.empty_cache()
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         p = make_problem(N, 2880, 201088, 64, 1.0, seed=args.seed, mask="frac", mask_frac=0.02,
                          device="cuda", name=f"sweep_{N}")
         torch.cuda.synchronize()
@@ -745,9 +748,15 @@ def run_sweep(args):
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
+        # cross-check on the device: the drop in free memory since before the problem
+        # was drawn (the caching allocator keeps its peak reservation) against torch's
+        # own peak; the library allocates nothing outside the caller's tensors
+        device_used = free0 - torch.cuda.mem_get_info()[0]
         print(json.dumps({"sweep": True, "N": N, "ms_per_step": ms, "tokens_per_s": N / (ms / 1e3),
                           "tflops": 8.0 * N * 2880 * 201088 / (ms / 1e3) / 1e12,
                           "peak_mem_gb": torch.cuda.max_memory_allocated() / 1e9,
+                          "peak_reserved_gb": torch.cuda.max_memory_reserved() / 1e9,
+                          "device_free_drop_gb": device_used / 1e9,
                           "workspace_gb": head.ws.numel() / 1e9,
                           "dense_grid_bf16_gb": N * 201088 * 2 / 1e9}), flush=True)
         del head, p
