@@ -127,6 +127,11 @@ def recorded_traffic(kernel: str, workload: str, chunk: int):
     return rec.get("bytes_per_launch", {}).get(kernel)
 
 
+def dense_grid_bytes(n_tokens: int, vocab: int, bytes_per_elem: int) -> int:
+    """Bytes of one dense tokens x vocabulary grid: what the fused head never allocates."""
+    return int(n_tokens) * int(vocab) * int(bytes_per_elem)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -758,7 +763,7 @@ def run_sweep(args):
                           "peak_reserved_gb": torch.cuda.max_memory_reserved() / 1e9,
                           "device_free_drop_gb": device_used / 1e9,
                           "workspace_gb": head.ws.numel() / 1e9,
-                          "dense_grid_bf16_gb": N * 201088 * 2 / 1e9}), flush=True)
+                          "dense_grid_bf16_gb": dense_grid_bytes(N, 201088, 2) / 1e9}), flush=True)
         del head, p
         torch.cuda.empty_cache()
 

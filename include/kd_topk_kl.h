@@ -21,9 +21,11 @@
  * The mean loss is sum(loss) / n_valid, formed by the caller.
  *
  * Conventions shared by every call:
- *   - All pointers are DEVICE pointers owned by the caller. The library never
- *     allocates, frees or synchronises (kd_get_status is the one exception:
- *     it synchronises the given stream).
+ *   - All pointers are DEVICE pointers owned by the caller, into memory of the
+ *     CURRENT device (cudaSetDevice) or managed memory; anything else (host
+ *     memory, another device's memory) is refused with KD_ERR_ARG before any
+ *     launch. The library never allocates, frees or synchronises
+ *     (kd_get_status is the one exception: it synchronises the given stream).
  *   - Every compute call is asynchronous on `stream` (a cudaStream_t; 0 is the
  *     legacy default stream).
  *   - Layouts are row-major and contiguous. bf16 tensors are passed as
@@ -49,7 +51,7 @@ extern "C" {
 
 typedef enum {
   KD_OK = 0,
-  KD_ERR_ARG = 1,          /* bad size, NULL pointer or bad T */
+  KD_ERR_ARG = 1,          /* bad size, NULL pointer, bad T, or memory not on the current device */
   KD_ERR_ALIGN = 2,        /* a pointer breaks the alignment rules above */
   KD_ERR_UNSUPPORTED = 3,  /* shape outside what the kernels handle, or no sm_103 device */
   KD_ERR_WORKSPACE = 4,    /* ws_bytes smaller than kd_topk_kl_workspace_size() */
@@ -102,6 +104,70 @@ kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const int32_t* to
                          const float* dloss, int64_t N, int D, int V, int K, float T,
                          int64_t chunk_tokens, int accumulate_dW, uint16_t* dH, float* dW,
                          void* ws, size_t ws_bytes, kd_stream_t stream);
+
+/*
+ * Upstream gradient of the mean loss, computed on the device from the count
+ * the forward wrote (no host round trip): dloss[n] = 1 / n_valid at counted
+ * rows (mask[n] != 0, or every row when mask is NULL) and 0 elsewhere, all 0
+ * when n_valid is 0 (reading: the mean over no rows is 0). loss_sum[0] (fp64,
+ * device) receives sum_n loss[n], summed in a fixed order. Either output may
+ * be NULL (loss may be NULL when loss_sum is). n_valid is a device int64; in
+ * token-sharded data parallelism it is the count summed over all ranks, so
+ * each rank's rows get the gradient of the global mean.
+ */
+kd_status kd_topk_kl_mean_grad(const float* loss, const uint8_t* mask, int64_t N,
+                               const int64_t* n_valid, float* dloss, double* loss_sum,
+                               kd_stream_t stream);
+
+/*
+ * Vocabulary shards: the head split over the vocabulary (W's rows), each shard
+ * held by one rank, as tensor-parallel heads are. The pages name multi-GPU
+ * communication as the method's open question (news article "Offline Top-K
+ * Distillation Removes the Need for a Resident Teacher Model...", closing
+ * caveats); this is the plainest split of the same computation: every
+ * per-row quantity is a sum or a logsumexp over vocabulary columns, so a shard
+ * computes its part and the parts are combined exactly.
+ *
+ * A shard covers ids [v0, v0 + V_shard) of a vocabulary of V; W_shard is
+ * those rows of W ([V_shard x D] bf16). topk_idx holds GLOBAL ids in [0, V)
+ * (checked as in kd_topk_kl_fwd); each shard uses the teacher entries that
+ * fall in its range, and the teacher softmax always runs over all K.
+ *
+ *   kd_topk_kl_fwd_shard: parts [N x 2] fp32 = per row (logsumexp over the
+ *     shard's columns of Z/T, sum_k P_k z_k over the teacher entries in the
+ *     shard, z unscaled), ent [N] fp32 = sum_j P_j log P_j of the row's
+ *     teacher grid (the same on every shard; 0 at masked rows), n_valid as in
+ *     kd_topk_kl_fwd.
+ *   kd_topk_kl_shard_merge: parts [R x N x 2] = the R shards' parts stacked in
+ *     shard order (e.g. an all-gather), ent from any shard -> loss [N] and
+ *     lse [N] exactly as kd_topk_kl_fwd defines them. Shards are combined in
+ *     index order, so every rank merging the same parts gets the same bits.
+ *   kd_topk_kl_bwd_shard: with the MERGED lse and dloss, the shard's part of
+ *     the gradients: dH [N x D] fp32 = dZ_shard W_shard (added to dH's
+ *     contents if accumulate_dH != 0; the full dH is the sum over shards) and
+ *     dW_shard [V_shard x D] fp32 = dZ_shard^T H (added if accumulate_dW).
+ *   ws: kd_topk_kl_shard_workspace_size(N, D, V_shard, K, chunk_tokens) bytes
+ *     (fwd and bwd of a shard).
+ * Layout, alignment and error rules are those of kd_topk_kl_fwd / _bwd;
+ * parts must be 8-byte aligned. A range outside [0, V) is KD_ERR_ARG.
+ */
+size_t kd_topk_kl_shard_workspace_size(int64_t N, int D, int V_shard, int K, int64_t chunk_tokens);
+
+kd_status kd_topk_kl_fwd_shard(const uint16_t* H, const uint16_t* W_shard, int v0, int V_shard,
+                               int V, const int32_t* topk_idx, const float* topk_logit,
+                               const uint8_t* mask, int64_t N, int D, int K, float T, float* parts,
+                               float* ent, int64_t* n_valid, void* ws, size_t ws_bytes,
+                               kd_stream_t stream);
+
+kd_status kd_topk_kl_shard_merge(const float* parts, int R, const float* ent, const uint8_t* mask,
+                                 int64_t N, float T, float* loss, float* lse, kd_stream_t stream);
+
+kd_status kd_topk_kl_bwd_shard(const uint16_t* H, const uint16_t* W_shard, int v0, int V_shard,
+                               int V, const int32_t* topk_idx, const float* topk_logit,
+                               const uint8_t* mask, const float* lse, const float* dloss,
+                               int64_t N, int D, int K, float T, int64_t chunk_tokens,
+                               int accumulate_dW, int accumulate_dH, float* dH, float* dW_shard,
+                               void* ws, size_t ws_bytes, kd_stream_t stream);
 
 /*
  * The loss from logits the caller has already computed, and optionally its
@@ -170,7 +236,9 @@ kd_status kd_teacher_topk(const uint16_t* H, const uint16_t* W, int64_t N, int D
  *     K = 64, V = 201,088. Larger sizes are rejected with KD_ERR_WORKSPACE
  *     before anything is launched.
  *   - The first call on each device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     that device current), and so does the first call after the device's
+ *     context has been replaced (cudaDeviceReset); make that first call before
+ *     any stream capture.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents (nothing in it has to start at zero: every cell a call reads is
  *     written earlier in that call). Calls that can overlap on the GPU, e.g. on

@@ -21,7 +21,7 @@ extern "C" {
  * a_mn = 0: A is [M x K] row-major (K contiguous); a_mn = 1: A is [K x M]
  * row-major (M contiguous). b_mn likewise for B ([N x K] or [K x N]).
  * C is [M x N] fp32 row-major. Device pointers, 16-byte aligned; M, N and K
- * must be multiples of 8. (a_mn, b_mn) = (1, 0) is not supported.
+ * must be multiples of 8.
  * cta_pair != 0 runs the CTA-pair form the loss uses (cta_group::2, 256-row
  * tiles); 0 runs the single-CTA form (128-row tiles).
  */
@@ -59,7 +59,8 @@ kd_status kd_debug_schedule(int kind, int64_t rows, int64_t cols, int64_t depth,
  * events and returns, per category, the summed milliseconds and the launch
  * count (arrays of length n; categories: 0 prep, 1 forward GEMM, 2 combine,
  * 3 dZ GEMM, 4 dH GEMM, 5 dH split sum, 6 dW GEMM, 7 loss from logits,
- * 8 teacher-logit GEMM, 9 top-K selection), then clears the records.
+ * 8 teacher-logit GEMM, 9 top-K selection, 10 transposes of W and H for the
+ * backward), then clears the records.
  * Event objects are created on first use and kept for the process lifetime.
  */
 kd_status kd_debug_profile(int enable);

@@ -2,7 +2,9 @@
 from .kd_oracle import (  # noqa: F401
     dense_teacher_grid,
     kd_backward,
+    kd_backward_shard,
     kd_forward,
+    kd_forward_shard,
     kd_from_logits,
     logsumexp_rows,
     mean_loss,

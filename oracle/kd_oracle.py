@@ -48,6 +48,8 @@ __all__ = [
     "dense_teacher_grid",
     "kd_from_logits",
     "teacher_topk",
+    "kd_forward_shard",
+    "kd_backward_shard",
 ]
 
 
@@ -228,3 +230,78 @@ def teacher_topk(H, W, K: int, row_chunk: int = 64):
         ids[r0:r1] = order
         vals[r0:r1] = np.take_along_axis(z, order, axis=1)
     return ids, vals
+
+
+def kd_forward_shard(H, W, idx, t, mask, T: float, v0: int, v1: int, row_chunk: int = 64):
+    """The per-row pieces of the loss that a slice [v0, v1) of the vocabulary holds.
+
+    The loss is a sum over vocabulary columns plus a logsumexp over them, so
+    it splits over any partition of the vocabulary (the pages leave multi-GPU
+    communication open: news article "Offline Top-K Distillation Removes the
+    Need for a Resident Teacher Model...", closing caveats). Per row n (fp64,
+    W the FULL [V x D] weight, only its rows v0..v1-1 used):
+      lse_s[n] = logsumexp_{v0 <= j < v1} (H[n] W[j]^T / T)
+      x_s[n]   = sum_{v0 <= j < v1} P[n, j] * (H[n] W[j]^T)     (0 on masked rows)
+      ent[n]   = sum_{j: P[n, j] > 0} P[n, j] log P[n, j]      (0 on masked rows)
+    with P the dense teacher grid of the whole vocabulary. Over a partition,
+    lse = logsumexp_s lse_s and loss = ent - (sum_s x_s) / T + lse.
+    Returns (lse_s[N], x_s[N], ent[N]).
+    """
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    idx = np.asarray(idx)
+    t = np.asarray(t)
+    mask = np.asarray(mask).astype(bool)
+    N, V = H.shape[0], W.shape[0]
+    lse_s = np.zeros(N, dtype=np.float64)
+    x_s = np.zeros(N, dtype=np.float64)
+    ent = np.zeros(N, dtype=np.float64)
+    for r0, r1 in _blocks(N, row_chunk):
+        z = student_logits(H[r0:r1], W[v0:v1])
+        lse_s[r0:r1] = logsumexp_rows(z / T)
+        valid = np.nonzero(mask[r0:r1])[0]
+        if valid.size == 0:
+            continue
+        P = dense_teacher_grid(idx[r0:r1][valid].astype(np.int64),
+                               teacher_log_probs(t[r0:r1][valid], T), V)
+        x_s[r0 + valid] = np.sum(P[:, v0:v1] * z[valid], axis=1)
+        pos = P > 0
+        terms = np.zeros_like(P)
+        terms[pos] = P[pos] * np.log(P[pos])
+        ent[r0 + valid] = np.sum(terms, axis=1)
+    return lse_s, x_s, ent
+
+
+def kd_backward_shard(H, W, idx, t, mask, T: float, g, lse, v0: int, v1: int, row_chunk: int = 64):
+    """The slice [v0, v1) of the vocabulary's share of the gradients.
+
+    With the logsumexp of the WHOLE vocabulary, lse[n], per row (fp64):
+      dZ_s[n, j] = (g_n / T) (exp(H[n] W[j]^T / T - lse[n]) - P[n, j])   for v0 <= j < v1
+    (0 on masked rows), and
+      dH_s = dZ_s W[v0:v1]      (the full dH is the sum over the slices)
+      dW_s = dZ_s^T H           (rows v0..v1-1 of the full dW)
+    Returns (dH_s[N, D], dW_s[v1 - v0, D]).
+    """
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    idx = np.asarray(idx)
+    t = np.asarray(t)
+    mask = np.asarray(mask).astype(bool)
+    g = np.asarray(g, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    N, D = H.shape
+    V = W.shape[0]
+    dH = np.zeros((N, D), dtype=np.float64)
+    dW = np.zeros((v1 - v0, D), dtype=np.float64)
+    for r0, r1 in _blocks(N, row_chunk):
+        valid = np.nonzero(mask[r0:r1])[0]
+        if valid.size == 0:
+            continue
+        rows = r0 + valid
+        z = student_logits(H[rows], W[v0:v1])
+        q = np.exp(z / T - lse[rows][:, None])
+        P = dense_teacher_grid(idx[rows].astype(np.int64), teacher_log_probs(t[rows], T), V)
+        dZ = (g[rows] / T)[:, None] * (q - P[:, v0:v1])
+        dH[rows] = dZ @ W[v0:v1]
+        dW += dZ.T @ H[rows]
+    return dH, dW

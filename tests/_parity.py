@@ -2,11 +2,14 @@
 run the CPU fp64 oracle on the same inputs, and compare with the tolerances
 the loss is specified to (bf16 operands, fp32 accumulation):
 
-  per-row loss and lse: |gpu - ref| <= 1e-3 |ref| + 1e-4 (absolute floor for
-                        rows whose loss is near 0)
-  mean loss:            relative 1e-3
-  dH, dW:               max|gpu - ref| / max|ref| <= 2e-2 and
-                        ||gpu - ref||_F / ||ref||_F <= 5e-3
+  per-row loss:  |gpu - ref| <= 1e-3 |ref| where |ref| >= 0.1, and <= 1e-4 nats
+                 where |ref| < 0.1 (a relative bound means nothing at a loss of 0;
+                 masked rows and rows whose teacher matches the student are there)
+  lse:           |gpu - ref| <= 1e-5 max(|ref|, 1): fp32 accumulation of the
+                 logits and of the sum of exponentials, nothing looser
+  mean loss:     relative 1e-3
+  dH, dW:        max|gpu - ref| / max|ref| <= 2e-2 and
+                 ||gpu - ref||_F / ||ref||_F <= 5e-3
 """
 from __future__ import annotations
 
@@ -18,7 +21,9 @@ from top_kl_loss_lm_b300 import binding
 from workloads import Problem, mean_upstream_grad
 
 LOSS_RTOL = 1e-3
+LOSS_FLOOR_BELOW = 0.1   # |ref| under this gets the absolute bound instead
 LOSS_ATOL = 1e-4
+LSE_RTOL = 1e-5
 GRAD_MAXREL = 2e-2
 GRAD_NORMREL = 5e-3
 
@@ -71,12 +76,25 @@ def run_oracle(p: Problem, g: np.ndarray = None, rows=None, backward=True):
 
 
 def assert_rows_close(got, ref, name):
+    """Per-row loss bound; returns how many rows were judged by the absolute floor."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(got - ref)
-    bound = LOSS_RTOL * np.abs(ref) + LOSS_ATOL
+    small = np.abs(ref) < LOSS_FLOOR_BELOW
+    bound = np.where(small, LOSS_ATOL, LOSS_RTOL * np.abs(ref))
     bad = np.nonzero(~(err <= bound))[0]
-    assert bad.size == 0, f"{name}: {bad.size} rows off, worst {err.max():.3e} at {int(np.argmax(err))}"
+    assert bad.size == 0, (f"{name}: {bad.size} rows off, worst {err.max():.3e} at {int(np.argmax(err))} "
+                           f"({int(small.sum())} of {ref.size} rows under the absolute floor)")
+    return int(small.sum())
+
+
+def assert_lse_close(got, ref, name="lse"):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    rel = err / np.maximum(np.abs(ref), 1.0)
+    bad = np.nonzero(~(rel <= LSE_RTOL))[0]
+    assert bad.size == 0, f"{name}: {bad.size} rows off, worst relative {rel.max():.3e}"
 
 
 def assert_grad_close(got, ref, name):
@@ -99,7 +117,7 @@ def compare_full(p: Problem, gpu: dict, backward=True):
     assert gpu["status"] == 0, binding.STATUS.get(gpu["status"])
     assert int(gpu["n_valid"].item()) == ref["n_valid"]
     assert_rows_close(gpu["loss"].cpu().numpy(), ref["loss"], "loss")
-    assert_rows_close(gpu["lse"].cpu().numpy(), ref["lse"], "lse")
+    assert_lse_close(gpu["lse"].cpu().numpy(), ref["lse"], "lse")
     nv = ref["n_valid"]
     gm = float(gpu["loss"].double().sum().item()) / nv if nv else 0.0
     rm = oracle.mean_loss(ref["loss"], nv)

@@ -82,9 +82,11 @@ def test_workspace_linear_in_tokens(lib):
     slopes = [(ws[i + 1] - ws[i]) / (Ns[i + 1] - Ns[i]) for i in range(1, len(Ns) - 1)]
     assert max(slopes) < 2 * 1024 and max(slopes) - min(slopes) < 64
     for n, w in zip(Ns, ws):
-        # at most two dZ chunks and the dH split partials (at most 8 x chunk x D
-        # fp32) are vocabulary- or chunk-sized, all fixed in N
-        assert w < 2 * 4096 * V * 2 + 8 * 4096 * D * 4 + n * 2048
+        # two dZ chunks, the transposed copies of W (V x D bf16) and of a dW
+        # group's H (2 chunks x D bf16) and the dH split partials (at most 8 x
+        # chunk x D fp32) are vocabulary- or chunk-sized, all fixed in N
+        fixed = 2 * 4096 * V * 2 + V * D * 2 + 2 * 4096 * D * 2 + 8 * 4096 * D * 4
+        assert w < fixed + n * 2048
         if n >= 65536:
             assert w < n * V * 2 / 3  # well below one dense N x V bf16 grid
     assert binding.kd_topk_kl_workspace_size(0, D, V, K, 0) > 0
@@ -139,3 +141,26 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         binding.kd_topk_kl_workspace_size(16, 8, 32, 2)
     with pytest.raises(RuntimeError, match="missing"):
         binding.lib()
+
+
+def test_binding_refuses_host_tensors_and_mixed_devices():
+    # the library launches on the current device and refuses other memory; the
+    # binding therefore needs every tensor of a call on one CUDA device and makes
+    # that device current around the call
+    from types import SimpleNamespace
+    N, D, V, K = 4, 8, 16, 2
+    H = torch.zeros(N, D, dtype=torch.bfloat16)
+    W = torch.zeros(V, D, dtype=torch.bfloat16)
+    idx = torch.zeros(N, K, dtype=torch.int32)
+    t = torch.zeros(N, K)
+    out = [torch.zeros(N), torch.zeros(N), torch.zeros(1, dtype=torch.int64)]
+    ws = torch.zeros(256, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        binding.kd_topk_kl_fwd(H, W, idx, t, None, 1.0, *out, ws)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        binding.kd_topk_kl_fwd_noalloc(H, W, idx, t, None, 1.0, *out)
+    a = SimpleNamespace(is_cuda=True, device=torch.device("cuda", 0))
+    b = SimpleNamespace(is_cuda=True, device=torch.device("cuda", 1))
+    assert binding.call_device(a, None, a) == torch.device("cuda", 0)
+    with pytest.raises(ValueError, match="different devices"):
+        binding.call_device(a, b)

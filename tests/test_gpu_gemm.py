@@ -1,8 +1,8 @@
 """The tcgen05/TMA mainloop on its own, as a plain GEMM against torch.matmul in
-fp32 on the same bf16 operands, for the three operand layouts the loss uses:
-both K-major (logits), B MN-major (dH = dZ W) and both MN-major (dW = dZ^T H),
-in the CTA-pair form (cta_group::2, 256-row tiles) the loss runs and in the
-single-CTA form.
+fp32 on the same bf16 operands, for every operand layout: both K-major (the
+logits, and dH = dZ W with W transposed), A MN-major with B K-major (dW = dZ^T H
+with H transposed), B MN-major and both MN-major, in the CTA-pair form
+(cta_group::2, 256-row tiles) the loss runs and in the single-CTA form.
 """
 import pytest
 import torch
@@ -19,7 +19,7 @@ def _ref(A, B, a_mn, b_mn):
 
 
 @pytest.mark.parametrize("cta_pair", [True, False])
-@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, True)])
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (True, False), (False, True), (True, True)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 128), (200, 264, 136),
                                    (128, 240, 64), (1024, 2880, 1024), (384, 1000, 8)])
 def test_gemm_matches_torch(a_mn, b_mn, M, N, K, cta_pair):

@@ -85,7 +85,7 @@ def test_no_counted_rows():
     assert torch.all(gpu["loss"] == 0)
     assert torch.all(gpu["dH"].float() == 0) and torch.all(gpu["dW"] == 0)
     ref = P.run_oracle(p, backward=False)
-    P.assert_rows_close(gpu["lse"].cpu().numpy(), ref["lse"], "lse")
+    P.assert_lse_close(gpu["lse"].cpu().numpy(), ref["lse"], "lse")
 
 
 def test_chunk_size_invariance():
@@ -175,13 +175,15 @@ def _check_sampled(p, chunk=0):
     ref = P.run_oracle(p, g, rows=rows, backward=True)
     assert int(gpu["n_valid"].item()) == int(p.mask.sum().item())
     P.assert_rows_close(gpu["loss"].cpu().numpy()[rows], ref["loss"], "loss (sampled rows)")
-    P.assert_rows_close(gpu["lse"].cpu().numpy()[rows], ref["lse"], "lse (sampled rows)")
+    P.assert_lse_close(gpu["lse"].cpu().numpy()[rows], ref["lse"], "lse (sampled rows)")
     P.assert_grad_close(gpu["dH"].double().cpu().numpy()[rows], ref["dH"], "dH (sampled rows)")
     # full-size property: sum_v dW[v, :] = sum_n (sum_j dZ[n, j]) H[n, :] = 0
     dW = gpu["dW"]
     assert torch.isfinite(dW).all()
-    colsum = dW.double().sum(0).abs().max().item()
-    assert colsum <= 1e-2 * dW.double().abs().sum(0).max().item()
+    # (what is left comes from rounding dZ to bf16 before the contraction: about
+    # 1e-6 of a column's absolute sum at these sizes)
+    ratio = dW.double().sum(0).abs().max().item() / dW.double().abs().sum(0).max().item()
+    assert ratio <= 1e-4, ratio
     # dW over the sampled rows alone: upstream gradient only there
     gs = torch.zeros_like(gpu["g"])
     gs[torch.as_tensor(rows, device=gs.device)] = gpu["g"][torch.as_tensor(rows, device=gs.device)]
@@ -232,4 +234,8 @@ def test_peak_memory_linear_in_tokens():
         torch.cuda.empty_cache()
     per_token = [(peaks[i + 1] - peaks[i]) / (Ns[i + 1] - Ns[i]) for i in range(len(Ns) - 1)]
     assert abs(per_token[1] - per_token[0]) <= 0.05 * per_token[0]
-    assert peaks[-1] < Ns[-1] * V * 2 / 4  # far below a single dense N x V bf16 grid
+    # a dense N x V bf16 grid costs V * 2 bytes per token; the fused head's growth is
+    # H, dH and the teacher cache (a few KB), and the fixed part (W, dW, W^T, the dZ
+    # chunks) is a small fraction of one grid at 65,536 tokens
+    assert per_token[-1] < 0.05 * V * 2
+    assert peaks[-1] < Ns[-1] * V * 2 / 3

@@ -289,8 +289,9 @@ def test_planted_mistakes_are_caught(monkeypatch, name, fn):
 
 
 def test_dense_grid_bytes_match_pages_example():
-    # The blog's worked size: a 4 x 201,088 x 32,768 bf16 teacher grid is
-    # "about 50GB" (fixture records the figures and where they are printed).
+    # The blog's worked size: a 4 x 201,088 x 32,768 bf16 teacher grid is about
+    # 50 GB (the fixture records the figures and where they are printed); the
+    # memory sweep of bench.py reports this size beside the fused head's peak.
     fx = {}
     with open(__file__.replace("test_oracle_pins.py", "golden/pages_dense_grid.txt")) as f:
         for line in f:
@@ -298,7 +299,7 @@ def test_dense_grid_bytes_match_pages_example():
             if line and not line.startswith("#"):
                 k, v = line.split()
                 fx[k] = float(v)
-    from top_kl_loss_lm_b300.memory import dense_grid_bytes
+    from bench import dense_grid_bytes
     b = dense_grid_bytes(int(fx["batch"]) * int(fx["seq"]), int(fx["vocab"]), int(fx["bytes_per_elem"]))
     assert b == 4 * 201088 * 32768 * 2
     assert abs(b / 1e9 - fx["approx_gb"]) / fx["approx_gb"] < 0.1
@@ -403,3 +404,56 @@ def test_teacher_topk_feeds_the_loss_at_k_equals_v():
     ids, vals = oracle.teacher_topk(H, W, 11)
     loss, _, _ = oracle.kd_forward(H, W, ids, vals, np.ones(3, dtype=np.uint8), 1.3)
     assert np.max(np.abs(loss)) < 1e-12
+
+
+# ----------------------------------------------------------------------------- vocabulary shards
+
+
+def _shard_problem():
+    # three uneven slices; row 1 repeats an id, row 3 is masked (NaN teacher logits)
+    H, W, idx, t, mask = _rand_problem(21, 7, 6, 23, 5, masked=(3,), dup_row=1)
+    t[3] = np.nan
+    idx[5] = [0, 1, 2, 3, 4]  # every teacher id of row 5 in the first slice
+    return H, W, idx, t, mask, [(0, 8), (8, 9), (9, 23)]
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_vocab_shards_recombine_to_the_whole_vocabulary(T):
+    # logsumexp and sums over a partition of the columns give back kd_forward /
+    # kd_backward exactly (up to fp64 rounding), for any split
+    H, W, idx, t, mask, cuts = _shard_problem()
+    loss, lse, _ = oracle.kd_forward(H, W, idx, t, mask, T)
+    g = np.linspace(0.3, 1.1, H.shape[0])
+    dH, dW = oracle.kd_backward(H, W, idx, t, mask, T, g)
+    parts = [oracle.kd_forward_shard(H, W, idx, t, mask, T, a, b) for a, b in cuts]
+    lse_m = np.logaddexp.reduce(np.stack([p[0] for p in parts]), axis=0)
+    x = np.sum([p[1] for p in parts], axis=0)
+    for p in parts:
+        np.testing.assert_array_equal(p[2], parts[0][2])  # entropy: the whole grid, every shard
+    loss_m = np.where(mask.astype(bool), parts[0][2] - x / T + lse_m, 0.0)
+    assert _rel(lse_m, lse) < 1e-13
+    assert _rel(loss_m, loss) < 1e-12
+    grads = [oracle.kd_backward_shard(H, W, idx, t, mask, T, g, lse, a, b) for a, b in cuts]
+    assert _rel(np.sum([gr[0] for gr in grads], axis=0), dH) < 1e-12
+    assert _rel(np.concatenate([gr[1] for gr in grads], axis=0), dW) < 1e-12
+
+
+def test_vocab_shard_pieces_match_torch():
+    # each piece on its own, by an independent route: torch's logsumexp over the
+    # slice, the dense grid filled entry by entry, -entr(P) summed for the entropy
+    T = 1.3
+    H, W, idx, t, mask, cuts = _shard_problem()
+    Z = torch.tensor(H) @ torch.tensor(W).T
+    for a, b in cuts:
+        lse_s, x_s, ent = oracle.kd_forward_shard(H, W, idx, t, mask, T, a, b)
+        np.testing.assert_allclose(lse_s, torch.logsumexp(Z[:, a:b] / T, dim=1).numpy(), rtol=1e-13)
+        for n in range(H.shape[0]):
+            if not mask[n]:
+                assert x_s[n] == 0.0 and ent[n] == 0.0
+                continue
+            pk = torch.softmax(torch.tensor(t[n]) / T, dim=0)
+            P = torch.zeros(W.shape[0], dtype=torch.float64)
+            for k in range(idx.shape[1]):
+                P[int(idx[n, k])] += pk[k]
+            assert x_s[n] == pytest.approx(float((P[a:b] * Z[n, a:b]).sum()), rel=1e-12, abs=1e-14)
+            assert ent[n] == pytest.approx(float(-torch.special.entr(P).sum()), rel=1e-12)

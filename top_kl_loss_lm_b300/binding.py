@@ -18,7 +18,9 @@ import torch
 __all__ = [
     "KdError", "lib", "library_path",
     "kd_topk_kl_workspace_size", "kd_topk_kl_fwd", "kd_topk_kl_bwd", "kd_topk_kl_fwd_noalloc",
-    "kd_topk_kl_logits_workspace_size", "kd_topk_kl_logits",
+    "kd_topk_kl_logits_workspace_size", "kd_topk_kl_logits", "kd_topk_kl_mean_grad",
+    "kd_topk_kl_shard_workspace_size", "kd_topk_kl_fwd_shard", "kd_topk_kl_shard_merge",
+    "kd_topk_kl_bwd_shard", "call_device",
     "kd_teacher_topk_workspace_size", "kd_teacher_topk",
     "kd_get_status", "kd_status_string",
     "kd_debug_gemm_bf16", "kd_debug_wait_timeout", "kd_debug_schedule",
@@ -67,6 +69,18 @@ def lib() -> ctypes.CDLL:
         L.kd_topk_kl_bwd.restype = i32
         L.kd_topk_kl_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp, vp]
         L.kd_topk_kl_fwd_noalloc.restype = i32
+        L.kd_topk_kl_mean_grad.argtypes = [vp, vp, i64, vp, vp, vp, vp]
+        L.kd_topk_kl_mean_grad.restype = i32
+        L.kd_topk_kl_shard_workspace_size.argtypes = [i64, i32, i32, i32, i64]
+        L.kd_topk_kl_shard_workspace_size.restype = sz
+        L.kd_topk_kl_fwd_shard.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, i64, i32, i32, f32, vp,
+                                           vp, vp, vp, sz, vp]
+        L.kd_topk_kl_fwd_shard.restype = i32
+        L.kd_topk_kl_shard_merge.argtypes = [vp, i32, vp, vp, i64, f32, vp, vp, vp]
+        L.kd_topk_kl_shard_merge.restype = i32
+        L.kd_topk_kl_bwd_shard.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, i64, i32, i32,
+                                           f32, i64, i32, i32, vp, vp, vp, sz, vp]
+        L.kd_topk_kl_bwd_shard.restype = i32
         L.kd_topk_kl_logits_workspace_size.argtypes = [i64, i32]
         L.kd_topk_kl_logits_workspace_size.restype = sz
         L.kd_topk_kl_logits.argtypes = [vp, i64, vp, vp, vp, vp, i64, i32, i32, f32, vp, vp, vp, vp,
@@ -94,12 +108,34 @@ def lib() -> ctypes.CDLL:
         return L
 
 
-def _stream(stream) -> Optional[int]:
+def _stream(stream, device=None) -> Optional[int]:
+    """The stream handle to launch on: the given one, else the current stream of
+    `device` (the device the call's tensors live on)."""
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(device).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)
+
+
+def call_device(*tensors) -> torch.device:
+    """The one CUDA device every given tensor (None entries skipped) lives on.
+
+    The library launches on the CURRENT device and refuses memory of any other,
+    so each wrapper makes this device current around its call."""
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"tensor on {t.device}: the library needs CUDA tensors")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"tensors on different devices ({dev} and {t.device})")
+    if dev is None:
+        raise ValueError("no tensor given")
+    return dev
 
 
 def _ptr(t: Optional[torch.Tensor], dtype, shape, name: str, device=None):
@@ -134,7 +170,7 @@ def kd_topk_kl_fwd(H, W, topk_idx, topk_logit, mask, T: float, loss, lse, n_vali
     N, D = H.shape
     V = W.shape[0]
     K = topk_idx.shape[1]
-    dev = H.device
+    dev = call_device(H, W, topk_idx, topk_logit, mask, loss, lse, n_valid, ws)
     args = (
         _ptr(H, torch.bfloat16, (N, D), "H", dev), _ptr(W, torch.bfloat16, (V, D), "W", dev),
         _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
@@ -143,9 +179,10 @@ def kd_topk_kl_fwd(H, W, topk_idx, topk_logit, mask, T: float, loss, lse, n_vali
         N, D, V, K, float(T),
         _ptr(loss, torch.float32, (N,), "loss", dev), _ptr(lse, torch.float32, (N,), "lse", dev),
         _ptr(n_valid, torch.int64, (1,), "n_valid", dev),
-        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream),
+        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream, dev),
     )
-    _check(lib().kd_topk_kl_fwd(*args), "kd_topk_kl_fwd")
+    with torch.cuda.device(dev):
+        _check(lib().kd_topk_kl_fwd(*args), "kd_topk_kl_fwd")
 
 
 def kd_topk_kl_fwd_noalloc(H, W, topk_idx, topk_logit, mask, T: float, loss, lse, n_valid,
@@ -158,7 +195,7 @@ def kd_topk_kl_fwd_noalloc(H, W, topk_idx, topk_logit, mask, T: float, loss, lse
     N, D = H.shape
     V = W.shape[0]
     K = topk_idx.shape[1]
-    dev = H.device
+    dev = call_device(H, W, topk_idx, topk_logit, mask, loss, lse, n_valid)
     args = (
         _ptr(H, torch.bfloat16, (N, D), "H", dev), _ptr(W, torch.bfloat16, (V, D), "W", dev),
         _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
@@ -166,9 +203,10 @@ def kd_topk_kl_fwd_noalloc(H, W, topk_idx, topk_logit, mask, T: float, loss, lse
         _ptr(mask, torch.uint8, (N,), "mask", dev),
         N, D, V, K, float(T),
         _ptr(loss, torch.float32, (N,), "loss", dev), _ptr(lse, torch.float32, (N,), "lse", dev),
-        _ptr(n_valid, torch.int64, (1,), "n_valid", dev), _stream(stream),
+        _ptr(n_valid, torch.int64, (1,), "n_valid", dev), _stream(stream, dev),
     )
-    _check(lib().kd_topk_kl_fwd_noalloc(*args), "kd_topk_kl_fwd_noalloc")
+    with torch.cuda.device(dev):
+        _check(lib().kd_topk_kl_fwd_noalloc(*args), "kd_topk_kl_fwd_noalloc")
 
 
 def kd_topk_kl_bwd(H, W, topk_idx, topk_logit, mask, lse, dloss, T: float, chunk_tokens: int,
@@ -177,7 +215,7 @@ def kd_topk_kl_bwd(H, W, topk_idx, topk_logit, mask, lse, dloss, T: float, chunk
     N, D = H.shape
     V = W.shape[0]
     K = topk_idx.shape[1]
-    dev = H.device
+    dev = call_device(H, W, topk_idx, topk_logit, mask, lse, dloss, dH, dW, ws)
     args = (
         _ptr(H, torch.bfloat16, (N, D), "H", dev), _ptr(W, torch.bfloat16, (V, D), "W", dev),
         _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
@@ -186,9 +224,85 @@ def kd_topk_kl_bwd(H, W, topk_idx, topk_logit, mask, lse, dloss, T: float, chunk
         _ptr(lse, torch.float32, (N,), "lse", dev), _ptr(dloss, torch.float32, (N,), "dloss", dev),
         N, D, V, K, float(T), int(chunk_tokens), 1 if accumulate_dW else 0,
         _ptr(dH, torch.bfloat16, (N, D), "dH", dev), _ptr(dW, torch.float32, (V, D), "dW", dev),
-        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream),
+        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream, dev),
     )
-    _check(lib().kd_topk_kl_bwd(*args), "kd_topk_kl_bwd")
+    with torch.cuda.device(dev):
+        _check(lib().kd_topk_kl_bwd(*args), "kd_topk_kl_bwd")
+
+
+def kd_topk_kl_mean_grad(loss, mask, n_valid, dloss=None, loss_sum=None, stream=None):
+    """dloss = mask / n_valid (n_valid read on the device) and loss_sum = sum(loss), fp64."""
+    N = loss.shape[0]
+    dev = call_device(loss, mask, n_valid, dloss, loss_sum)
+    args = (
+        _ptr(loss, torch.float32, (N,), "loss", dev), _ptr(mask, torch.uint8, (N,), "mask", dev), N,
+        _ptr(n_valid, torch.int64, (1,), "n_valid", dev), _ptr(dloss, torch.float32, (N,), "dloss", dev),
+        _ptr(loss_sum, torch.float64, (1,), "loss_sum", dev), _stream(stream, dev),
+    )
+    with torch.cuda.device(dev):
+        _check(lib().kd_topk_kl_mean_grad(*args), "kd_topk_kl_mean_grad")
+
+
+def kd_topk_kl_shard_workspace_size(N: int, D: int, V_shard: int, K: int, chunk_tokens: int = 0) -> int:
+    return int(lib().kd_topk_kl_shard_workspace_size(N, D, V_shard, K, chunk_tokens))
+
+
+def kd_topk_kl_fwd_shard(H, W_shard, v0: int, V: int, topk_idx, topk_logit, mask, T: float, parts,
+                         ent, n_valid, ws, stream=None):
+    """Forward of the vocabulary shard [v0, v0 + W_shard.shape[0]) of V: parts [N, 2], ent [N]."""
+    N, D = H.shape
+    Vs = W_shard.shape[0]
+    K = topk_idx.shape[1]
+    dev = call_device(H, W_shard, topk_idx, topk_logit, mask, parts, ent, n_valid, ws)
+    args = (
+        _ptr(H, torch.bfloat16, (N, D), "H", dev), _ptr(W_shard, torch.bfloat16, (Vs, D), "W_shard", dev),
+        int(v0), Vs, int(V),
+        _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
+        _ptr(topk_logit, torch.float32, (N, K), "topk_logit", dev),
+        _ptr(mask, torch.uint8, (N,), "mask", dev), N, D, K, float(T),
+        _ptr(parts, torch.float32, (N, 2), "parts", dev), _ptr(ent, torch.float32, (N,), "ent", dev),
+        _ptr(n_valid, torch.int64, (1,), "n_valid", dev),
+        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream, dev),
+    )
+    with torch.cuda.device(dev):
+        _check(lib().kd_topk_kl_fwd_shard(*args), "kd_topk_kl_fwd_shard")
+
+
+def kd_topk_kl_shard_merge(parts, ent, mask, T: float, loss, lse, stream=None):
+    """loss, lse [N] from the shards' parts stacked as [R, N, 2] (shard order)."""
+    R, N = parts.shape[0], parts.shape[1]
+    dev = call_device(parts, ent, mask, loss, lse)
+    args = (
+        _ptr(parts, torch.float32, (R, N, 2), "parts", dev), R,
+        _ptr(ent, torch.float32, (N,), "ent", dev), _ptr(mask, torch.uint8, (N,), "mask", dev), N,
+        float(T), _ptr(loss, torch.float32, (N,), "loss", dev), _ptr(lse, torch.float32, (N,), "lse", dev),
+        _stream(stream, dev),
+    )
+    with torch.cuda.device(dev):
+        _check(lib().kd_topk_kl_shard_merge(*args), "kd_topk_kl_shard_merge")
+
+
+def kd_topk_kl_bwd_shard(H, W_shard, v0: int, V: int, topk_idx, topk_logit, mask, lse, dloss,
+                         T: float, chunk_tokens: int, accumulate_dW: bool, accumulate_dH: bool, dH,
+                         dW_shard, ws, stream=None):
+    """The shard's gradients: dH [N, D] fp32 (its part of the sum over shards), dW_shard fp32."""
+    N, D = H.shape
+    Vs = W_shard.shape[0]
+    K = topk_idx.shape[1]
+    dev = call_device(H, W_shard, topk_idx, topk_logit, mask, lse, dloss, dH, dW_shard, ws)
+    args = (
+        _ptr(H, torch.bfloat16, (N, D), "H", dev), _ptr(W_shard, torch.bfloat16, (Vs, D), "W_shard", dev),
+        int(v0), Vs, int(V),
+        _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
+        _ptr(topk_logit, torch.float32, (N, K), "topk_logit", dev),
+        _ptr(mask, torch.uint8, (N,), "mask", dev),
+        _ptr(lse, torch.float32, (N,), "lse", dev), _ptr(dloss, torch.float32, (N,), "dloss", dev),
+        N, D, K, float(T), int(chunk_tokens), 1 if accumulate_dW else 0, 1 if accumulate_dH else 0,
+        _ptr(dH, torch.float32, (N, D), "dH", dev), _ptr(dW_shard, torch.float32, (Vs, D), "dW_shard", dev),
+        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream, dev),
+    )
+    with torch.cuda.device(dev):
+        _check(lib().kd_topk_kl_bwd_shard(*args), "kd_topk_kl_bwd_shard")
 
 
 def kd_topk_kl_logits_workspace_size(N: int, K: int) -> int:
@@ -211,7 +325,7 @@ def kd_topk_kl_logits(Z, topk_idx, topk_logit, mask, T: float, loss, lse, n_vali
     """Loss (and dZ when dloss and dZ are given) from materialised bf16 logits Z [N x V]."""
     N, V = Z.shape
     K = topk_idx.shape[1]
-    dev = Z.device
+    dev = call_device(Z, topk_idx, topk_logit, mask, loss, lse, n_valid, ws, dloss, dZ)
     zp, ldz = _rows_ptr(Z, "Z", N, V, dev)
     dp, lddz = (None, 0) if dZ is None else _rows_ptr(dZ, "dZ", N, V, dev)
     args = (
@@ -222,9 +336,10 @@ def kd_topk_kl_logits(Z, topk_idx, topk_logit, mask, T: float, loss, lse, n_vali
         N, V, K, float(T),
         _ptr(loss, torch.float32, (N,), "loss", dev), _ptr(lse, torch.float32, (N,), "lse", dev),
         _ptr(n_valid, torch.int64, (1,), "n_valid", dev), dp, lddz,
-        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream),
+        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream, dev),
     )
-    _check(lib().kd_topk_kl_logits(*args), "kd_topk_kl_logits")
+    with torch.cuda.device(dev):
+        _check(lib().kd_topk_kl_logits(*args), "kd_topk_kl_logits")
 
 
 def kd_teacher_topk_workspace_size(N: int, D: int, V: int, K: int) -> int:
@@ -236,20 +351,24 @@ def kd_teacher_topk(H, W, topk_idx, topk_logit, ws, stream=None):
     N, D = H.shape
     V = W.shape[0]
     K = topk_idx.shape[1]
-    dev = H.device
+    dev = call_device(H, W, topk_idx, topk_logit, ws)
     args = (
         _ptr(H, torch.bfloat16, (N, D), "H", dev), _ptr(W, torch.bfloat16, (V, D), "W", dev),
         N, D, V, K,
         _ptr(topk_idx, torch.int32, (N, K), "topk_idx", dev),
         _ptr(topk_logit, torch.float32, (N, K), "topk_logit", dev),
-        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream),
+        _ptr(ws, torch.uint8, (ws.numel(),), "ws", dev), ws.numel(), _stream(stream, dev),
     )
-    _check(lib().kd_teacher_topk(*args), "kd_teacher_topk")
+    with torch.cuda.device(dev):
+        _check(lib().kd_teacher_topk(*args), "kd_teacher_topk")
 
 
-def kd_get_status(stream=None) -> int:
-    """Synchronise the stream and return (and clear) the device status word."""
-    return int(lib().kd_get_status(_stream(stream)))
+def kd_get_status(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the status word of `device`
+    (default: the current device)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().kd_get_status(_stream(stream, dev)))
 
 
 def kd_debug_gemm_bf16(A, B, C, a_mn: bool, b_mn: bool, cta_pair: bool = True, stream=None):
@@ -259,13 +378,14 @@ def kd_debug_gemm_bf16(A, B, C, a_mn: bool, b_mn: bool, cta_pair: bool = True, s
     else:
         M, K = A.shape
     N = B.shape[1] if b_mn else B.shape[0]
-    dev = A.device
+    dev = call_device(A, B, C)
     _ptr(A, torch.bfloat16, tuple(A.shape), "A", dev)
     _ptr(B, torch.bfloat16, tuple(B.shape), "B", dev)
     _ptr(C, torch.float32, (M, N), "C", dev)
-    _check(lib().kd_debug_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
-                                    int(a_mn), int(b_mn), int(cta_pair), _stream(stream)),
-           "kd_debug_gemm_bf16")
+    with torch.cuda.device(dev):
+        _check(lib().kd_debug_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                        int(a_mn), int(b_mn), int(cta_pair), _stream(stream, dev)),
+               "kd_debug_gemm_bf16")
 
 
 def kd_debug_wait_timeout(timeout_ns: int, stream=None):
@@ -293,7 +413,7 @@ def kd_debug_schedule(kind: int, rows: int, cols: int, depth: int, grid_units: i
 
 
 PROFILE_CATEGORIES = ["prep", "fwd_gemm", "combine", "dz_gemm", "dh_gemm", "dh_sum", "dw_gemm",
-                      "logits", "topk_gemm", "topk_select"]
+                      "logits", "topk_gemm", "topk_select", "transpose"]
 
 
 def kd_debug_profile(enable: bool):

@@ -101,13 +101,15 @@ struct GemmArgs {
   int out_slot_rows;    // dh partials: rows of one k-split slice in the tmC tensor
   int* status;
   uint64_t timeout_ns;
+  int dh_partials;      // dH: fp32 partials through tmC even without a k-split
 };
 
 // fp32 tiles leave through tmC (TMA store, or TMA add for an accumulating dW):
-// dW, the plain GEMM, and the dH k-split partials.
+// dW, the plain GEMM, and the dH partials (k-split, or an fp32 dH).
 template <int EPI>
 __host__ __device__ __forceinline__ bool uses_tma_out(const GemmArgs& a) {
-  return EPI == kEpiDz || EPI == kEpiDw || EPI == kEpiPlain || (EPI == kEpiDh && a.sched.KS > 1);
+  return EPI == kEpiDz || EPI == kEpiDw || EPI == kEpiPlain ||
+         (EPI == kEpiDh && (a.sched.KS > 1 || a.dh_partials != 0));
 }
 
 // One 32-column TMEM chunk of a warp's 32 rows -> two swizzled 32 x 16 fp32 boxes

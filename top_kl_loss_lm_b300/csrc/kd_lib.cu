@@ -17,6 +17,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <vector>
 
@@ -39,6 +40,8 @@ constexpr int kMaxDevices = 64;
 struct DevInfo {
   bool ready = false;
   bool ok = false;
+  unsigned long long ctx_id = 0;  // the CUDA context the values below belong to
+  int dev = 0;
   int num_sms = 0;
   int pair_slots = 0;     // CTA pairs of the GEMM kernel that fit on the device at once
   int* status = nullptr;  // device address of g_kd_status
@@ -52,10 +55,41 @@ std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// Driver entry points used to tell CUDA contexts apart: a device's cached
+// addresses (the status word, the allocation-free forward's scratch) belong to
+// the context that was current when they were looked up, and are looked up
+// again when that context has gone (cudaDeviceReset) and another has replaced it.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+
+void* driver_entry(const char* name, unsigned version) {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return fn;
+  cudaGetLastError();
+  return nullptr;
+}
+
+// Unique id of the calling thread's current context; 0 when there is none yet
+// (the runtime creates the device's primary context on its first real use).
+unsigned long long current_ctx_id() {
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!g_ctx_current || !g_ctx_id || g_ctx_current(&c) != CUDA_SUCCESS || c == nullptr ||
+      g_ctx_id(c, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 // Optional per-launch timing (test hook kd_debug_profile): a start/stop event
 // pair recorded on the launching stream around every kernel of the library.
 enum ProfCat : int { kProfPrep = 0, kProfFwdGemm, kProfCombine, kProfDzGemm, kProfDhGemm, kProfDhSum,
-                     kProfDwGemm, kProfLogits, kProfTopkGemm, kProfTopkSelect, kProfCats };
+                     kProfDwGemm, kProfLogits, kProfTopkGemm, kProfTopkSelect, kProfTranspose,
+                     kProfCats };
 struct Prof {
   bool on = false;
   std::vector<cudaEvent_t> ev;      // pool: 2 per record
@@ -97,9 +131,21 @@ const DevInfo* device_info(kd_status* err) {
     return nullptr;
   }
   std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_ctx_current) {
+    g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(driver_entry("cuCtxGetCurrent", 4000));
+    g_ctx_id = reinterpret_cast<CtxGetIdFn>(driver_entry("cuCtxGetId", 12000));
+  }
   DevInfo& d = g_dev[dev];
-  if (!d.ready) {
+  unsigned long long cur = current_ctx_id();
+  if (cur == 0 && d.ready) {
+    // no current context, e.g. after cudaDeviceReset: have the runtime set up the
+    // device's primary context now, so that it can be told apart from the old one
+    if (cudaSetDevice(dev) == cudaSuccess) cur = current_ctx_id();
+    cudaGetLastError();
+  }
+  if (!d.ready || cur != d.ctx_id) {
     d.ready = true;
+    d.dev = dev;
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -107,14 +153,9 @@ const DevInfo* device_info(kd_status* err) {
     void* p = nullptr;
     const bool sym = cudaGetSymbolAddress(&p, g_kd_status) == cudaSuccess;
     d.status = static_cast<int*>(p);
-    if (!g_encode) {
-      cudaDriverEntryPointQueryResult q;
-      void* fn = nullptr;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q) == cudaSuccess &&
-          q == cudaDriverEntryPointSuccess)
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
+    if (!g_encode)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(
+          driver_entry("cuTensorMapEncodeTiled", 12000));
     d.ok = sym && g_encode != nullptr && major == 10 && minor == 3 && d.num_sms > 0;
     d.pair_slots = d.num_sms / 2;
     if (d.ok) {
@@ -139,6 +180,7 @@ const DevInfo* device_info(kd_status* err) {
       }
     }
     cudaGetLastError();
+    d.ctx_id = current_ctx_id();  // the symbol lookup above made the context current
   }
   if (!d.ok) {
     *err = KD_ERR_UNSUPPORTED;
@@ -189,7 +231,8 @@ struct Layout {
   // forward
   size_t part = 0, zk = 0;
   // backward
-  size_t dz = 0, dhp = 0;
+  size_t dz = 0, ht = 0, dhp = 0;
+  int64_t ldht = 0;  // row stride (elements) of the transposed H copy
   size_t fwd_end = 0, bwd_end = 0, total = 0;
   int slots = 0;
   int64_t C = 0, C_pad = 0, dz_ld = 0;
@@ -201,6 +244,7 @@ struct Layout {
 // all their tokens: half as many read-add-write passes over the fp32 dW.
 constexpr int kDwGroup = 2;
 constexpr int kMaxDwGroup = 4;
+
 
 Layout plan(int64_t N, int D, int V, int K, int64_t chunk) {
   Layout L;
@@ -231,6 +275,10 @@ Layout plan(int64_t N, int D, int V, int K, int64_t chunk) {
   L.G = static_cast<int>(cdiv(N, C) < kDwGroup ? (cdiv(N, C) < 1 ? 1 : cdiv(N, C)) : kDwGroup);
   L.dz = off;
   off = align256(off + static_cast<size_t>(L.G) * L.C_pad * L.dz_ld * sizeof(uint16_t));
+  // the dW group's H^T [D x G*C]: the K-major B operand of dW
+  L.ldht = static_cast<int64_t>(L.G) * L.C_pad;
+  L.ht = off;
+  off = align256(off + static_cast<size_t>(D) * L.ldht * sizeof(uint16_t));
   L.dhp = off;  // k-split partials of dH take whatever follows (sized at call time)
   L.bwd_end = off;
   L.total = L.fwd_end > L.bwd_end ? L.fwd_end : L.bwd_end;
@@ -259,6 +307,16 @@ int wanted_ksplit(int64_t C_pad, int D, int V, int grid) {
 kd_status cuda_check() {
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
+// dst [C x R] = transpose of src [R x C] (bf16; C a multiple of 8).
+kd_status launch_transpose(const uint16_t* src, int64_t R, int C, int64_t lds, uint16_t* dst,
+                           int64_t ldd, cudaStream_t s) {
+  if (R <= 0) return KD_OK;
+  ProfScope ps(kProfTranspose, s);
+  const dim3 grid(static_cast<unsigned>(cdiv(R, kTrTile)), static_cast<unsigned>(cdiv(C, kTrTile)));
+  kd_transpose_kernel<<<grid, 256, 0, s>>>(src, R, C, lds, dst, ldd);
+  return cuda_check();
 }
 
 template <int EPI, bool AMN, bool BMN, bool PAIR>
@@ -309,6 +367,22 @@ GemmArgs base_args(const DevInfo* di) {
   return a;
 }
 
+// Whether every non-NULL pointer in the list addresses memory the current device
+// can use: device memory of that device, or managed memory.
+bool on_device(const DevInfo* di, std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs) {
+    if (p == nullptr) continue;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (a.type == cudaMemoryTypeManaged) continue;
+    if (a.type != cudaMemoryTypeDevice || a.device != di->dev) return false;
+  }
+  return true;
+}
+
 kd_status check_common(const uint16_t* H, const uint16_t* W, const int32_t* idx, const float* t,
                        int64_t N, int D, int V, int K, float T, const void* ws) {
   if (N < 0 || D <= 0 || V <= 0 || K < 1 || K > kMaxTopK) return KD_ERR_ARG;
@@ -327,9 +401,19 @@ kd_status check_common(const uint16_t* H, const uint16_t* W, const int32_t* idx,
 
 using namespace kd;
 
-extern "C" size_t kd_topk_kl_workspace_size(int64_t N, int D, int V, int K, int64_t chunk_tokens) {
-  if (N < 0 || D <= 0 || V <= 0 || K < 1 || K > kMaxTopK || D % 8 != 0) return 0;
-  Layout L = plan(N, D, V, K, chunk_tokens);
+namespace kd {
+namespace {
+
+// The vocabulary columns a call covers: ids [v0, v0 + Vs) of a vocabulary of V
+// (the whole vocabulary is v0 = 0, Vs = V; a vocabulary shard of W otherwise).
+struct VRange {
+  int v0, Vs, V;
+};
+
+// Workspace bytes for the forward and backward over Vs vocabulary columns. An
+// fp32 dH (a vocabulary shard's partial) needs at least one slice of partials.
+size_t workspace_bytes(int64_t N, int D, int Vs, int K, int64_t chunk, bool dh_f32) {
+  Layout L = plan(N, D, Vs, K, chunk);
   int sms = 148;
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) {
@@ -337,31 +421,29 @@ extern "C" size_t kd_topk_kl_workspace_size(int64_t N, int D, int V, int K, int6
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) sms = n;
   }
   cudaGetLastError();
-  const int ks = wanted_ksplit(L.C_pad, D, V, kPair ? sms / 2 : sms);
+  const int ks = wanted_ksplit(L.C_pad, D, Vs, kPair ? sms / 2 : sms);
   size_t bwd = L.bwd_end;
-  if (ks > 1) bwd = align256(L.dhp + static_cast<size_t>(ks) * L.C_pad * D * sizeof(float));
+  if (ks > 1 || dh_f32) bwd = align256(L.dhp + static_cast<size_t>(ks) * L.C_pad * D * sizeof(float));
   return L.fwd_end > bwd ? L.fwd_end : bwd;
 }
 
-extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
-                                    const float* topk_logit, const uint8_t* mask, int64_t N, int D,
-                                    int V, int K, float T, float* loss, float* lse,
-                                    int64_t* n_valid, void* ws, size_t ws_bytes,
-                                    kd_stream_t stream) {
-  kd_status st = check_common(H, W, topk_idx, topk_logit, N, D, V, K, T, ws);
-  if (st != KD_OK) return st;
-  if (!n_valid || (N > 0 && (!loss || !lse))) return KD_ERR_ARG;
-  if (!aligned(n_valid, 8) || !aligned(loss, 4) || !aligned(lse, 4)) return KD_ERR_ALIGN;
-  const DevInfo* di = device_info(&st);
-  if (!di) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+// Forward over the columns of vr. Whole vocabulary: loss and lse per row. A
+// shard (shard_out set): per row (lse over the shard, sum_k P_k z_k over the
+// shard's teacher entries) into shard_out and the teacher grid's entropy into
+// ent_out; loss and lse are not written.
+kd_status fwd_run(const DevInfo* di, const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                  const float* topk_logit, const uint8_t* mask, int64_t N, int D, VRange vr, int K,
+                  float T, float* loss, float* lse, int64_t* n_valid, float2* shard_out,
+                  float* ent_out, void* ws, size_t ws_bytes, cudaStream_t s) {
+  kd_status st = KD_OK;
   if (cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s) != cudaSuccess) return KD_ERR_CUDA;
   if (N == 0) return KD_OK;
+  const int V = vr.Vs;  // the GEMM's vocabulary columns
   const Layout L = plan(N, D, V, K, 0);
   if (ws_bytes < L.fwd_end) return KD_ERR_WORKSPACE;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int2* pairs = reinterpret_cast<int2*>(w + L.pairs);
-  float* ent = reinterpret_cast<float*>(w + L.ent);
+  float* ent = ent_out ? ent_out : reinterpret_cast<float*>(w + L.ent);
   float2* part = reinterpret_cast<float2*>(w + L.part);
   float* zk = reinterpret_cast<float*>(w + L.zk);
   const float inv_T = 1.0f / T;
@@ -369,7 +451,7 @@ extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const 
   {
     ProfScope ps(kProfPrep, s);
     kd_prep_kernel<<<static_cast<unsigned>(cdiv(N, kPrepWarps)), kPrepWarps * 32, 0, s>>>(
-        topk_idx, topk_logit, mask, N, K, V, inv_T, pairs, ent,
+        topk_idx, topk_logit, mask, N, K, vr.V, vr.v0, vr.Vs, inv_T, pairs, ent,
         reinterpret_cast<unsigned long long*>(n_valid), di->status);
   }
   if ((st = cuda_check()) != KD_OK) return st;
@@ -410,33 +492,35 @@ extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const 
   {
     ProfScope ps(kProfCombine, s);
     kd_combine_kernel<<<static_cast<unsigned>(cdiv(N, 256)), 256, 0, s>>>(
-        last_start, S_full, S_last, part, L.slots, pairs, zk, ent, mask, N, K, V, inv_T, loss, lse);
+        last_start, S_full, S_last, part, L.slots, pairs, zk, ent, mask, N, K, V, inv_T, loss, lse,
+        shard_out);
   }
   return cuda_check();
 }
 
-extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
-                                    const float* topk_logit, const uint8_t* mask, const float* lse,
-                                    const float* dloss, int64_t N, int D, int V, int K, float T,
-                                    int64_t chunk_tokens, int accumulate_dW, uint16_t* dH,
-                                    float* dW, void* ws, size_t ws_bytes, kd_stream_t stream) {
-  kd_status st = check_common(H, W, topk_idx, topk_logit, N, D, V, K, T, ws);
-  if (st != KD_OK) return st;
-  if (!dW || (N > 0 && (!lse || !dloss || !dH))) return KD_ERR_ARG;
-  if (!aligned(dW, 16) || !aligned(dH, 16) || !aligned(lse, 4) || !aligned(dloss, 4))
-    return KD_ERR_ALIGN;
-  const DevInfo* di = device_info(&st);
-  if (!di) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+// Backward over the columns of vr. dH is written as bf16 (dH) or, for a
+// vocabulary shard's partial, as fp32 (dH_f32, added to its contents if
+// accumulate_dH); dW covers the vr.Vs columns.
+kd_status bwd_run(const DevInfo* di, const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                  const float* topk_logit, const uint8_t* mask, const float* lse,
+                  const float* dloss, int64_t N, int D, VRange vr, int K, float T,
+                  int64_t chunk_tokens, int accumulate_dW, uint16_t* dH, float* dH_f32,
+                  int accumulate_dH, float* dW, void* ws, size_t ws_bytes, cudaStream_t s) {
+  kd_status st = KD_OK;
+  const int V = vr.Vs;  // the GEMMs' vocabulary columns
   if (N == 0) {
     if (!accumulate_dW &&
         cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * D * sizeof(float), s) != cudaSuccess)
       return KD_ERR_CUDA;
     return KD_OK;
   }
+  const bool f32 = dH_f32 != nullptr;
   const Layout L = plan(N, D, V, K, chunk_tokens);
   if (ws_bytes < L.bwd_end) return KD_ERR_WORKSPACE;
+  const size_t slice = static_cast<size_t>(L.C_pad) * D * sizeof(float);
+  if (f32 && ws_bytes < L.dhp + slice) return KD_ERR_WORKSPACE;
   const int KS = ksplit_that_fits(L, D, ws_bytes, wanted_ksplit(L.C_pad, D, V, gemm_slots(di)));
+  const bool partials = KS > 1 || f32;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int2* pairs = reinterpret_cast<int2*>(w + L.pairs);
   float* ent = reinterpret_cast<float*>(w + L.ent);
@@ -447,14 +531,24 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
   {
     ProfScope ps(kProfPrep, s);
     kd_prep_kernel<<<static_cast<unsigned>(cdiv(N, kPrepWarps)), kPrepWarps * 32, 0, s>>>(
-        topk_idx, topk_logit, mask, N, K, V, inv_T, pairs, ent, nullptr, di->status);
+        topk_idx, topk_logit, mask, N, K, vr.V, vr.v0, vr.Vs, inv_T, pairs, ent, nullptr,
+        di->status);
   }
   if ((st = cuda_check()) != KD_OK) return st;
 
-  const int BNd = hidden_tile_width(D);
-  const int NBd = static_cast<int>(cdiv(D, BNd));
+  // dH: B = W, MN-major, 256-wide hidden tiles (zero fill past D). dW: B = the
+  // group's H^T, K-major, even hidden tiles (no padded columns). The transposed
+  // copy of the 8,192-token group costs ~0.03 ms and made dW ~8% faster than
+  // reading H MN-major with 256-wide padded tiles; a transposed W for dH gained
+  // less than its transpose cost.
+  const int BNh = mn_major_tile_width(D);
+  const int NBh = static_cast<int>(cdiv(D, BNh));
+  const int BNw = hidden_tile_width(D);
+  const int NBw = static_cast<int>(cdiv(D, BNw));
   if (L.G < 1 || L.G > kMaxDwGroup) return KD_ERR_UNSUPPORTED;
-  CUtensorMap mH_k, mW_k, mW_mn, mDz_mn, mH_mn;
+  uint16_t* ht = reinterpret_cast<uint16_t*>(w + L.ht);
+
+  CUtensorMap mH_k, mW_k, mW_mn, mDz_mn;
   CUtensorMap mDz_k[kMaxDwGroup], mDz_out[kMaxDwGroup];  // one per dZ slot
   const uint64_t rowH = static_cast<uint64_t>(D) * 2;
   const uint64_t rowDz = static_cast<uint64_t>(L.dz_ld) * 2;
@@ -462,8 +556,7 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
   if (!make_map(&mH_k, H, D, N, rowH, kBK, kBM) ||
       !make_map(&mW_k, W, D, V, rowH, kBK, Geo<kPair>::kBRows) ||
       !make_map(&mW_mn, W, D, V, rowH, 64, kBK) ||
-      !make_map(&mDz_mn, dz, V, static_cast<uint64_t>(L.G) * L.C_pad, rowDz, 64, kBK) ||
-      !make_map(&mH_mn, H, D, N, rowH, 64, kBK))
+      !make_map(&mDz_mn, dz, V, static_cast<uint64_t>(L.G) * L.C_pad, rowDz, 64, kBK))
     return KD_ERR_CUDA;
   for (int g = 0; g < L.G; ++g)
     if (!make_map(&mDz_k[g], dz + g * slot_elems, V, L.C_pad, rowDz, kBK, kBM) ||
@@ -471,10 +564,10 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
       return KD_ERR_CUDA;
   CUtensorMap mDw_out, mDhp_out;
   if (!make_out_map(&mDw_out, dW, D, V, static_cast<uint64_t>(D) * 4) ||
-      (KS > 1 && !make_out_map(&mDhp_out, dhp, D, static_cast<uint64_t>(KS) * L.C_pad,
-                               static_cast<uint64_t>(D) * 4)))
+      (partials && !make_out_map(&mDhp_out, dhp, D, static_cast<uint64_t>(KS) * L.C_pad,
+                                 static_cast<uint64_t>(D) * 4)))
     return KD_ERR_CUDA;
-  if (KS <= 1) mDhp_out = mDw_out;  // unused: dH is written in bf16 directly
+  if (!partials) mDhp_out = mDw_out;  // unused: dH is written in bf16 directly
 
   const int KBd = static_cast<int>(cdiv(D, kBK));
   const int KBv = static_cast<int>(cdiv(V, kBK));
@@ -514,53 +607,206 @@ extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const 
 
     // 2. dH rows of the chunk = dZ W (contraction over V, split KS ways)
     GemmArgs h = base_args(di);
-    h.sched = make_tile_sched(MBc, NBd, KBv, KS);
+    h.sched = make_tile_sched(MBc, NBh, KBv, KS);
     h.M = static_cast<int>(rows);
     h.Ncols = D;
-    h.BN = BNd;
-    h.idesc = umma_idesc_bf16(kTileRows, BNd, false, true);
+    h.BN = BNh;
+    h.idesc = umma_idesc_bf16(kTileRows, BNh, false, true);
     h.row_base = c0;
     h.out_bf16 = dH;
     h.out_f32 = dhp;
     h.part_stride = L.C_pad * static_cast<int64_t>(D);
     h.out_slot_rows = static_cast<int>(L.C_pad);
+    h.dh_partials = f32 ? 1 : 0;
     {
       ProfScope ps(kProfDhGemm, s);
       if ((st = launch_gemm<kEpiDh, false, true, kPair>(mDz_k[slot], mW_mn, mDhp_out, h, di, s)) !=
           KD_OK)
         return st;
     }
-    if (h.sched.KS > 1) {
+    if (partials) {
       const int64_t groups = rows * (D / 8);
       int64_t blocks = cdiv(groups, 256);
       if (blocks > 8L * di->num_sms) blocks = 8L * di->num_sms;
       ProfScope ps(kProfDhSum, s);
-      kd_dh_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-          dhp, h.sched.KS, h.part_stride, rows, D, dH + c0 * D);
+      if (f32)
+        kd_dh_sum_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+            dhp, h.sched.KS, h.part_stride, rows, D, dH_f32 + c0 * D, accumulate_dH);
+      else
+        kd_dh_sum_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+            dhp, h.sched.KS, h.part_stride, rows, D, dH + c0 * D, 0);
       if ((st = cuda_check()) != KD_OK) return st;
     }
 
    }
     // 3. dW (+)= dZ^T H over the group's tokens: slot g's rows are tokens
     //    g0 + g*C + t, so the stacked slots are the group's tokens in order (rows
-    //    past the end of a short last chunk were stored as zeros)
+    //    past the end of a short last chunk were stored as zeros). B is the
+    //    group's H^T [D x tokens]; its map ends at the group's last token, so the
+    //    k-blocks past it read zeros.
+    if ((st = launch_transpose(H + g0 * D, group_rows, D, D, ht, L.ldht, s)) != KD_OK) return st;
+    CUtensorMap mHt_k;
+    if (!make_map(&mHt_k, ht, group_rows, D, static_cast<uint64_t>(L.ldht) * 2, kBK,
+                  Geo<kPair>::kBRows))
+      return KD_ERR_CUDA;
     GemmArgs g = base_args(di);
-    g.sched = make_tile_sched(MBv, NBd, static_cast<int>(cdiv(group_rows, kBK)), 1);
+    g.sched = make_tile_sched(MBv, NBw, static_cast<int>(cdiv(group_rows, kBK)), 1);
     g.M = V;
     g.Ncols = D;
-    g.BN = BNd;
-    g.idesc = umma_idesc_bf16(kTileRows, BNd, true, true);
-    g.b_k_off = static_cast<int>(g0);
+    g.BN = BNw;
+    g.idesc = umma_idesc_bf16(kTileRows, BNw, true, false);
     g.out_f32 = dW;
     g.ld_out = D;
     g.accumulate = (g0 > 0 || accumulate_dW) ? 1 : 0;
     {
       ProfScope ps(kProfDwGemm, s);
-      if ((st = launch_gemm<kEpiDw, true, true, kPair>(mDz_mn, mH_mn, mDw_out, g, di, s)) != KD_OK)
+      if ((st = launch_gemm<kEpiDw, true, false, kPair>(mDz_mn, mHt_k, mDw_out, g, di, s)) != KD_OK)
         return st;
     }
   }
   return KD_OK;
+}
+
+// Checks shared by the vocabulary-shard calls: the range lies in [0, V).
+bool shard_range_ok(int v0, int V_shard, int V) {
+  return v0 >= 0 && V_shard >= 1 && V_shard <= V && v0 <= V - V_shard;
+}
+
+}  // namespace
+}  // namespace kd
+
+extern "C" size_t kd_topk_kl_workspace_size(int64_t N, int D, int V, int K, int64_t chunk_tokens) {
+  if (N < 0 || D <= 0 || V <= 0 || K < 1 || K > kMaxTopK || D % 8 != 0) return 0;
+  return workspace_bytes(N, D, V, K, chunk_tokens, false);
+}
+
+extern "C" kd_status kd_topk_kl_fwd(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                                    const float* topk_logit, const uint8_t* mask, int64_t N, int D,
+                                    int V, int K, float T, float* loss, float* lse,
+                                    int64_t* n_valid, void* ws, size_t ws_bytes,
+                                    kd_stream_t stream) {
+  kd_status st = check_common(H, W, topk_idx, topk_logit, N, D, V, K, T, ws);
+  if (st != KD_OK) return st;
+  if (!n_valid || (N > 0 && (!loss || !lse))) return KD_ERR_ARG;
+  if (!aligned(n_valid, 8) || !aligned(loss, 4) || !aligned(lse, 4)) return KD_ERR_ALIGN;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  if (!on_device(di, {n_valid}) ||
+      (N > 0 && !on_device(di, {H, W, topk_idx, topk_logit, mask, loss, lse, ws})))
+    return KD_ERR_ARG;
+  return fwd_run(di, H, W, topk_idx, topk_logit, mask, N, D, VRange{0, V, V}, K, T, loss, lse,
+                 n_valid, nullptr, nullptr, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" kd_status kd_topk_kl_bwd(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                                    const float* topk_logit, const uint8_t* mask, const float* lse,
+                                    const float* dloss, int64_t N, int D, int V, int K, float T,
+                                    int64_t chunk_tokens, int accumulate_dW, uint16_t* dH,
+                                    float* dW, void* ws, size_t ws_bytes, kd_stream_t stream) {
+  kd_status st = check_common(H, W, topk_idx, topk_logit, N, D, V, K, T, ws);
+  if (st != KD_OK) return st;
+  if (!dW || (N > 0 && (!lse || !dloss || !dH))) return KD_ERR_ARG;
+  if (!aligned(dW, 16) || !aligned(dH, 16) || !aligned(lse, 4) || !aligned(dloss, 4))
+    return KD_ERR_ALIGN;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  if (!on_device(di, {dW}) ||
+      (N > 0 && !on_device(di, {H, W, topk_idx, topk_logit, mask, lse, dloss, dH, ws})))
+    return KD_ERR_ARG;
+  return bwd_run(di, H, W, topk_idx, topk_logit, mask, lse, dloss, N, D, VRange{0, V, V}, K, T,
+                 chunk_tokens, accumulate_dW, dH, nullptr, 0, dW, ws, ws_bytes,
+                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ vocabulary shards
+
+extern "C" size_t kd_topk_kl_shard_workspace_size(int64_t N, int D, int V_shard, int K,
+                                                  int64_t chunk_tokens) {
+  if (N < 0 || D <= 0 || V_shard <= 0 || K < 1 || K > kMaxTopK || D % 8 != 0) return 0;
+  return workspace_bytes(N, D, V_shard, K, chunk_tokens, true);
+}
+
+extern "C" kd_status kd_topk_kl_fwd_shard(const uint16_t* H, const uint16_t* W_shard, int v0,
+                                          int V_shard, int V, const int32_t* topk_idx,
+                                          const float* topk_logit, const uint8_t* mask, int64_t N,
+                                          int D, int K, float T, float* parts, float* ent,
+                                          int64_t* n_valid, void* ws, size_t ws_bytes,
+                                          kd_stream_t stream) {
+  kd_status st = check_common(H, W_shard, topk_idx, topk_logit, N, D, V, K, T, ws);
+  if (st != KD_OK) return st;
+  if (!shard_range_ok(v0, V_shard, V)) return KD_ERR_ARG;
+  if (!n_valid || (N > 0 && (!parts || !ent))) return KD_ERR_ARG;
+  if (!aligned(n_valid, 8) || !aligned(parts, 8) || !aligned(ent, 4)) return KD_ERR_ALIGN;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  if (!on_device(di, {n_valid}) ||
+      (N > 0 && !on_device(di, {H, W_shard, topk_idx, topk_logit, mask, parts, ent, ws})))
+    return KD_ERR_ARG;
+  return fwd_run(di, H, W_shard, topk_idx, topk_logit, mask, N, D, VRange{v0, V_shard, V}, K, T,
+                 nullptr, nullptr, n_valid, reinterpret_cast<float2*>(parts), ent, ws, ws_bytes,
+                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" kd_status kd_topk_kl_shard_merge(const float* parts, int R, const float* ent,
+                                            const uint8_t* mask, int64_t N, float T, float* loss,
+                                            float* lse, kd_stream_t stream) {
+  if (N < 0 || R < 1 || !(T > 0.0f) || !std::isfinite(T)) return KD_ERR_ARG;
+  if (N == 0) return KD_OK;
+  if (!parts || !ent || !loss || !lse) return KD_ERR_ARG;
+  if (!aligned(parts, 8) || !aligned(ent, 4) || !aligned(loss, 4) || !aligned(lse, 4))
+    return KD_ERR_ALIGN;
+  kd_status st = KD_OK;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  if (!on_device(di, {parts, ent, mask, loss, lse})) return KD_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  ProfScope ps(kProfCombine, s);
+  kd_shard_merge_kernel<<<static_cast<unsigned>(cdiv(N, 256)), 256, 0, s>>>(
+      reinterpret_cast<const float2*>(parts), R, ent, mask, N, 1.0f / T, loss, lse);
+  return cuda_check();
+}
+
+extern "C" kd_status kd_topk_kl_bwd_shard(const uint16_t* H, const uint16_t* W_shard, int v0,
+                                          int V_shard, int V, const int32_t* topk_idx,
+                                          const float* topk_logit, const uint8_t* mask,
+                                          const float* lse, const float* dloss, int64_t N, int D,
+                                          int K, float T, int64_t chunk_tokens, int accumulate_dW,
+                                          int accumulate_dH, float* dH, float* dW_shard, void* ws,
+                                          size_t ws_bytes, kd_stream_t stream) {
+  kd_status st = check_common(H, W_shard, topk_idx, topk_logit, N, D, V, K, T, ws);
+  if (st != KD_OK) return st;
+  if (!shard_range_ok(v0, V_shard, V)) return KD_ERR_ARG;
+  if (!dW_shard || (N > 0 && (!lse || !dloss || !dH))) return KD_ERR_ARG;
+  if (!aligned(dW_shard, 16) || !aligned(dH, 16) || !aligned(lse, 4) || !aligned(dloss, 4))
+    return KD_ERR_ALIGN;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  if (!on_device(di, {dW_shard}) ||
+      (N > 0 && !on_device(di, {H, W_shard, topk_idx, topk_logit, mask, lse, dloss, dH, ws})))
+    return KD_ERR_ARG;
+  return bwd_run(di, H, W_shard, topk_idx, topk_logit, mask, lse, dloss, N, D,
+                 VRange{v0, V_shard, V}, K, T, chunk_tokens, accumulate_dW, nullptr, dH,
+                 accumulate_dH, dW_shard, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ mean-loss gradient
+
+extern "C" kd_status kd_topk_kl_mean_grad(const float* loss, const uint8_t* mask, int64_t N,
+                                          const int64_t* n_valid, float* dloss, double* loss_sum,
+                                          kd_stream_t stream) {
+  if (N < 0 || !n_valid || (!dloss && !loss_sum) || (loss_sum && N > 0 && !loss))
+    return KD_ERR_ARG;
+  if (!aligned(n_valid, 8) || !aligned(loss, 4) || !aligned(dloss, 4) || !aligned(loss_sum, 8))
+    return KD_ERR_ALIGN;
+  kd_status st = KD_OK;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
+  if (!on_device(di, {loss, mask, n_valid, dloss, loss_sum})) return KD_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  ProfScope ps(kProfCombine, s);
+  kd_mean_grad_kernel<<<1, kMeanThreads, 0, s>>>(loss_sum ? loss : nullptr, mask, N, n_valid, dloss,
+                                                  loss_sum);
+  return cuda_check();
 }
 
 // ------------------------------------------------------------------ loss from materialised logits
@@ -666,6 +912,9 @@ extern "C" kd_status kd_topk_kl_logits(const uint16_t* Z, int64_t ldz, const int
   kd_status st = KD_OK;
   const DevInfo* di = device_info(&st);
   if (!di) return st;
+  if (!on_device(di, {n_valid}) ||
+      (N > 0 && !on_device(di, {Z, topk_idx, topk_logit, mask, dloss, loss, lse, dZ, ws})))
+    return KD_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s) != cudaSuccess) return KD_ERR_CUDA;
   if (N == 0) return KD_OK;
@@ -677,7 +926,7 @@ extern "C" kd_status kd_topk_kl_logits(const uint16_t* Z, int64_t ldz, const int
   {
     ProfScope ps(kProfPrep, s);
     kd_prep_kernel<<<static_cast<unsigned>(cdiv(N, kPrepWarps)), kPrepWarps * 32, 0, s>>>(
-        topk_idx, topk_logit, mask, N, K, V, inv_T, pairs, ent,
+        topk_idx, topk_logit, mask, N, K, V, 0, V, inv_T, pairs, ent,
         reinterpret_cast<unsigned long long*>(n_valid), di->status);
   }
   if ((st = cuda_check()) != KD_OK) return st;
@@ -768,6 +1017,7 @@ extern "C" kd_status kd_teacher_topk(const uint16_t* H, const uint16_t* W, int64
   kd_status st = KD_OK;
   const DevInfo* di = device_info(&st);
   if (!di) return st;
+  if (!on_device(di, {H, W, topk_idx, topk_logit, ws})) return KD_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t C = topk_chunk_rows(N);
   const int64_t ldz = topk_ld(V);
@@ -822,7 +1072,7 @@ extern "C" kd_status kd_get_status(kd_stream_t stream) {
 extern "C" const char* kd_status_string(kd_status status) {
   switch (status) {
     case KD_OK: return "ok";
-    case KD_ERR_ARG: return "invalid argument (size, NULL pointer or temperature)";
+    case KD_ERR_ARG: return "invalid argument (size, NULL pointer, temperature, or memory not on the current device)";
     case KD_ERR_ALIGN: return "pointer alignment violates the ABI rules";
     case KD_ERR_UNSUPPORTED: return "unsupported shape or device (needs an sm_103 GPU)";
     case KD_ERR_WORKSPACE: return "workspace smaller than kd_topk_kl_workspace_size()";
@@ -840,15 +1090,17 @@ extern "C" kd_status kd_debug_gemm_bf16(const uint16_t* A, const uint16_t* B, fl
   if (M <= 0 || N <= 0 || K <= 0 || M % 8 || N % 8 || K % 8) return KD_ERR_ARG;
   if (!A || !B || !C) return KD_ERR_ARG;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return KD_ERR_ALIGN;
-  if (a_mn && !b_mn) return KD_ERR_UNSUPPORTED;
   kd_status st = KD_OK;
   const DevInfo* di = device_info(&st);
   if (!di) return st;
+  if (!on_device(di, {A, B, C})) return KD_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool pair = cta_pair != 0;
   const int rows = pair ? Geo<true>::kTileRows : Geo<false>::kTileRows;
   const int b_rows = pair ? Geo<true>::kBRows : Geo<false>::kBRows;
-  const int BN = b_mn ? hidden_tile_width(N) : kBNMax;
+  // K-major B: the even split of the dH / dW products (e.g. 12 x 240 for N = 2,880);
+  // MN-major B: see mn_major_tile_width
+  const int BN = b_mn ? mn_major_tile_width(N) : hidden_tile_width(N);
   CUtensorMap ma, mb;
   bool ok;
   if (!a_mn)
@@ -874,10 +1126,12 @@ extern "C" kd_status kd_debug_gemm_bf16(const uint16_t* A, const uint16_t* B, fl
   if (pair) {
     if (!a_mn && !b_mn) return launch_gemm<kEpiPlain, false, false, true>(ma, mb, mc, a, di, s);
     if (!a_mn && b_mn) return launch_gemm<kEpiPlain, false, true, true>(ma, mb, mc, a, di, s);
+    if (a_mn && !b_mn) return launch_gemm<kEpiPlain, true, false, true>(ma, mb, mc, a, di, s);
     return launch_gemm<kEpiPlain, true, true, true>(ma, mb, mc, a, di, s);
   }
   if (!a_mn && !b_mn) return launch_gemm<kEpiPlain, false, false, false>(ma, mb, mc, a, di, s);
   if (!a_mn && b_mn) return launch_gemm<kEpiPlain, false, true, false>(ma, mb, mc, a, di, s);
+  if (a_mn && !b_mn) return launch_gemm<kEpiPlain, true, false, false>(ma, mb, mc, a, di, s);
   return launch_gemm<kEpiPlain, true, true, false>(ma, mb, mc, a, di, s);
 }
 
@@ -982,7 +1236,11 @@ static __device__ __align__(256) unsigned char g_kd_fwd_scratch[kFwdScratchBytes
 
 namespace {
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[kd::kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx = 0;  // context the address was looked up in
+  void* ptr = nullptr;
+};
+ScratchAddr g_scratch[kd::kMaxDevices];
 }  // namespace
 
 extern "C" kd_status kd_topk_kl_fwd_noalloc(const uint16_t* H, const uint16_t* W,
@@ -992,25 +1250,26 @@ extern "C" kd_status kd_topk_kl_fwd_noalloc(const uint16_t* H, const uint16_t* W
                                             kd_stream_t stream) {
   if (N < 0 || D <= 0 || V <= 0 || K < 1 || K > kMaxTopK || D % 8 != 0) return KD_ERR_ARG;
   if (plan(N, D, V, K, 0).fwd_end > kFwdScratchBytes) return KD_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kd::kMaxDevices) {
-    cudaGetLastError();
-    return KD_ERR_CUDA;
-  }
+  kd_status st = KD_OK;
+  const DevInfo* di = device_info(&st);
+  if (!di) return st;
   void* ws = nullptr;
   {
-    // Set-up once per device, with that device current: the host-side name of
-    // the array is not a device address, so ask the runtime for the real one.
+    // Set-up once per device (again if the device's context was replaced), with
+    // that device current: the host-side name of the array is not a device
+    // address, so ask the runtime for the real one.
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    ScratchAddr& sa = g_scratch[di->dev];
+    if (sa.ptr == nullptr || sa.ctx != di->ctx_id) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_kd_fwd_scratch) != cudaSuccess || p == nullptr) {
         cudaGetLastError();
         return KD_ERR_CUDA;
       }
-      g_scratch_ptr[dev] = p;
+      sa.ptr = p;
+      sa.ctx = di->ctx_id;
     }
-    ws = g_scratch_ptr[dev];
+    ws = sa.ptr;
   }
   return kd_topk_kl_fwd(H, W, topk_idx, topk_logit, mask, N, D, V, K, T, loss, lse, n_valid, ws,
                         kFwdScratchBytes, stream);

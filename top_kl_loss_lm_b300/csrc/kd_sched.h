@@ -142,15 +142,25 @@ inline int choose_ksplit(int64_t tiles, int KB, int grid) {
   return best;
 }
 
-// Column tile width over the hidden size D. Above 256 the tiles are 256 wide
-// and the last one is padded with zero-filled columns: with CTA pairs each CTA
-// then loads 128-column (256-byte) slabs that start on 128-byte boundaries,
-// while an even split such as 12 x 240 for D = 2,880 starts every other slab
-// mid-line and measured about 9% slower than 12 x 256 despite the padding.
-// A single tile (D <= 256) is D rounded up to a multiple of 16.
+// Column tile width over the hidden size D for a K-major B operand (dW, whose B
+// is the token group's H transposed): D is split evenly into ceil(D / 256)
+// tiles, each rounded up to a multiple of 16, e.g. 12 x 240 for D = 2,880
+// instead of 12 x 256 with 192 zero-filled columns. Each CTA of a pair then
+// holds 120 rows of B, a multiple of the 8-row core matrix.
 inline int hidden_tile_width(int D) {
-  if (D > kBNMax) return kBNMax;
-  return (D + 15) / 16 * 16;
+  const int nt = (D + kBNMax - 1) / kBNMax;
+  const int w = (D + nt - 1) / nt;
+  return (w + 15) / 16 * 16;
+}
+
+// Column tile width for an MN-major B operand (dH, whose B is W [V x D]): 256
+// above 256 columns, so every 64-column slab a CTA loads starts on a 128-byte
+// line (an even split such as 240 would start every other slab mid-line and
+// measured about 9% slower per useful FLOP); a single tile is N rounded up to a
+// multiple of 16.
+inline int mn_major_tile_width(int N) {
+  if (N > kBNMax) return kBNMax;
+  return (N + 15) / 16 * 16;
 }
 
 }  // namespace kd
