@@ -1,8 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of the fused top-K KL distillation head (forward + backward).
 
-One step = one forward (kd_topk_kl_fwd) and one backward (kd_topk_kl_bwd) over
-one batch of synthetic inputs of the named workload, all in the CUDA library.
+One step = forward (kd_topk_kl_fwd), the mean-loss gradient on the device
+(kd_topk_kl_mean_grad) and backward (kd_topk_kl_bwd) over one batch of
+synthetic inputs of the named workload, all in the CUDA library, driven by the
+product's token-sharded step (top_kl_loss_lm_b300.sharded.TokenShardedHead).
 Default workload: the long-context gpt-oss-shaped head, N = 32,768 tokens
 (batch 1 x seq 32,768), D = 2,880, V = 201,088, K = 64, T = 1, 2% of rows masked.
 
@@ -10,9 +12,11 @@ Default workload: the long-context gpt-oss-shaped head, N = 32,768 tokens
   python bench.py --impl reference ...   # the CPU fp64 oracle, timed on host cores
   python bench.py --sweep                # peak memory and rate for N = 4K ... 256K
 
-Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an
-independent replica on its own GPU (the head needs no exchange between
-replicas); the barrier-bracketed time is the max over ranks.
+Prints one JSON line (rank 0). With N > 1 (torchrun, one rank per GPU) the
+ranks run data parallelism over a global batch of N x 32,768 tokens: each rank
+its own 32,768 (weak scaling), the count of counted rows all-reduced before
+the backward and dW (V x D fp32) and the loss sum all-reduced after it, inside
+the timed step (NCCL). The barrier-bracketed time is the max over ranks.
 """
 from __future__ import annotations
 
@@ -56,12 +60,12 @@ def parse():
     ap.add_argument("--teacher-topk", action="store_true",
                     help="measure the teacher top-K cache producer (kd_teacher_topk) instead")
     ap.add_argument("--traffic-from", default=None,
-                    help="write the per-launch DRAM traffic record from this ncu --csv log and exit")
+                    help="write the per-launch DRAM traffic record of --workload (the small "
+                         "profiling case) from these comma-separated ncu --csv logs and exit")
     return ap.parse_args()
 
 
-def traffic_file(workload: str) -> str:
-    return os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.json")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "dram_traffic_profile_medium.json")
 KERNEL_SOURCES = ("kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h", "kd_logits.cuh", "kd_topk_cache.cuh")
 # template argument of kd_gemm_kernel -> category of the library's launch timing
 GEMM_EPI = {"0": "fwd_gemm", "1": "dz_gemm", "2": "dh_gemm", "3": "dw_gemm", "4": "topk_gemm"}
@@ -82,49 +86,75 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_from_ncu_csv(csv_path: str, workload: str, chunk: int) -> dict:
-    """DRAM bytes per launch of each GEMM kernel from an ncu --csv log holding
-    dram__bytes_read.sum and dram__bytes_write.sum."""
-    import csv
+def kernel_category(name: str):
     import re
-    per = {}
-    hdr = None
-    with open(csv_path) as f:
-        for r in csv.reader(f):
-            if r and r[0] == "ID":
-                hdr = r
-                continue
-            if hdr is None or len(r) < len(hdr):
-                continue
-            d = dict(zip(hdr, r))
-            m = re.search(r"kd_gemm_kernel<(\d)", d["Kernel Name"])
-            name = d["Kernel Name"]
-            cat = (GEMM_EPI[m.group(1)] if m else "logits" if "kd_logits_kernel" in name
-                   else "topk_select" if "kd_topk_select_kernel" in name else None)
-            if cat is None or d["Metric Name"] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
-                continue
-            unit = d.get("Metric Unit", "byte").lower()
-            scale = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9}.get(unit, 1)
-            v = float(d["Metric Value"].replace(",", "")) * scale
-            per.setdefault(cat, {}).setdefault(d["ID"], 0.0)
-            per[cat][d["ID"]] += v
-    return {"source_hash": kernel_source_hash(), "workload": workload, "chunk_tokens": chunk,
-            "bytes_per_launch": {k: sum(v.values()) / len(v) for k, v in per.items()},
-            "launches": {k: len(v) for k, v in per.items()}}
+    m = re.search(r"kd_gemm_kernel<(\d)", name)
+    if m:
+        return GEMM_EPI[m.group(1)]
+    for key, cat in (("kd_logits_kernel", "logits"), ("kd_topk_select_kernel", "topk_select"),
+                     ("kd_transpose_kernel", "transpose")):
+        if key in name:
+            return cat
+    return None
 
 
-def recorded_traffic(kernel: str, workload: str, chunk: int):
-    """DRAM bytes per launch recorded for this kernel, or None when the record is
-    missing, for another workload, or taken from different kernel sources."""
+def traffic_from_ncu_csv(csv_paths, workload: str, chunk: int) -> dict:
+    """DRAM bytes of every captured launch (dram__bytes_read.sum + dram__bytes_write.sum),
+    in capture order, from ncu --csv logs of the small profiling case."""
+    import csv
+    launches = {}
+    for path in csv_paths:
+        hdr = None
+        with open(path) as f:
+            for r in csv.reader(f):
+                if r and r[0] == "ID":
+                    hdr = r
+                    continue
+                if hdr is None or len(r) < len(hdr):
+                    continue
+                d = dict(zip(hdr, r))
+                cat = kernel_category(d["Kernel Name"])
+                if cat is None or d["Metric Name"] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                    continue
+                unit = d.get("Metric Unit", "byte").lower()
+                scale = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9}.get(unit, 1)
+                key = (path, int(d["ID"]))
+                e = launches.setdefault(key, {"cat": cat, "bytes": 0.0})
+                e["bytes"] += float(d["Metric Value"].replace(",", "")) * scale
+    from workloads import CONFIGS
+    case = dict(CONFIGS[workload], chunk_tokens=chunk)
+    return {"source_hash": kernel_source_hash(), "workload": workload, "case": case,
+            "launches": [launches[k] for k in sorted(launches)]}
+
+
+def recorded_traffic(kernel: str, p, chunk: int):
+    """DRAM bytes per launch of `kernel` at the bench's workload, scaled from the
+    small-case record, or None when the record is missing, was taken from other
+    kernel sources, or its case does not have the bench's D, K and launch sizes.
+
+    The small case runs the same launches (4,096 rows per forward / dZ / dH
+    launch, 8,192 tokens per dW launch) over a smaller vocabulary, so a launch's
+    traffic scales with V. dW's first launch of a step stores and the later ones
+    add: the per-launch figure weights the captured store and add launches as
+    the bench's step does."""
     try:
-        with open(traffic_file(workload)) as f:
+        with open(TRAFFIC_RECORD) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if (rec.get("source_hash") != kernel_source_hash() or rec.get("workload") != workload
-            or rec.get("chunk_tokens") != chunk):
+    case = rec.get("case", {})
+    if (rec.get("source_hash") != kernel_source_hash() or case.get("D") != p.D
+            or case.get("K") != p.K or case.get("chunk_tokens") != chunk):
         return None
-    return rec.get("bytes_per_launch", {}).get(kernel)
+    got = [x["bytes"] for x in rec.get("launches", []) if x["cat"] == kernel]
+    if not got:
+        return None
+    if kernel == "dw_gemm" and len(got) >= 2:
+        groups = -(-p.N // (2 * chunk))
+        per = (got[0] + (groups - 1) * (sum(got[1:]) / len(got[1:]))) / groups
+    else:
+        per = sum(got) / len(got)
+    return per * p.V / case["V"]
 
 
 def dense_grid_bytes(n_tokens: int, vocab: int, bytes_per_elem: int) -> int:
@@ -238,79 +268,74 @@ def dist_setup(args):
 
 # ---------------------------------------------------------------------- CPU oracle
 
-def oracle_rate(p, seconds: float, seed: int = 0, max_rows: int = 1024):
-    """Oracle fwd+bwd on a seeded sample of rows; returns (tokens/s, rows, secs, threads)."""
-    import numpy as np
+ORACLE_ROWS_PER_CALL = 64   # the same batch for the in-line cpu_baseline and --impl reference
 
-    import oracle
 
-    W64 = p.W.double().cpu().numpy()           # input conversion, outside the timed part
-    H = p.H.cpu()
-    m = p.mask.cpu().numpy()
-    idx = p.idx.cpu().numpy()
-    t = p.t.double().cpu().numpy()
-    nv = max(int(m.sum()), 1)
-    rng = np.random.default_rng(seed)
-
-    def run(n):
-        rows = np.sort(rng.choice(p.N, size=min(n, p.N), replace=False))
-        Hs = H[rows].double().numpy()
-        g = m[rows].astype(np.float64) / nv
-        t0 = time.perf_counter()
-        oracle.kd_forward(Hs, W64, idx[rows], t[rows], m[rows], p.T)
-        oracle.kd_backward(Hs, W64, idx[rows], t[rows], m[rows], p.T, g)
-        return len(rows), time.perf_counter() - t0
-
-    run(8)                       # first call pays BLAS start-up; not timed
-    n1, s1 = 0, 0.0
-    # batches of 128 rows until the time target (each call also writes a full V x D
-    # dW, so small batches would mostly time that)
-    while s1 < seconds and n1 < max_rows:
-        n, s = run(128)
-        n1 += n
-        s1 += s
+def oracle_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
-        threads = max(int(d.get("num_threads", 1)) for d in threadpool_info()) or os.cpu_count()
+        return max(int(d.get("num_threads", 1)) for d in threadpool_info()) or os.cpu_count()
     except Exception:
-        threads = os.cpu_count()
-    return n1 / s1, n1, s1, threads
+        return os.cpu_count()
+
+
+class OracleSample:
+    """The CPU oracle (fwd + bwd over the full vocabulary) on seeded samples of a
+    workload's rows, ORACLE_ROWS_PER_CALL rows a call. The oracle is row-additive,
+    so rows per second is its tokens per second."""
+
+    def __init__(self, p, seed: int = 0):
+        import numpy as np
+        self.np = np
+        self.p = p
+        self.W64 = p.W.double().cpu().numpy()      # input conversion, outside the timed part
+        self.H = p.H.cpu()
+        self.m = p.mask.cpu().numpy()
+        self.idx = p.idx.cpu().numpy()
+        self.t = p.t.double().cpu().numpy()
+        self.nv = max(int(self.m.sum()), 1)
+        self.rng = np.random.default_rng(seed)
+
+    def call(self) -> float:
+        """One oracle call on a fresh sample; returns its seconds."""
+        import oracle
+        np, p = self.np, self.p
+        rows = np.sort(self.rng.choice(p.N, size=min(ORACLE_ROWS_PER_CALL, p.N), replace=False))
+        Hs = self.H[rows].double().numpy()
+        t0 = time.perf_counter()
+        oracle.kd_forward(Hs, self.W64, self.idx[rows], self.t[rows], self.m[rows], p.T)
+        oracle.kd_backward(Hs, self.W64, self.idx[rows], self.t[rows], self.m[rows], p.T,
+                           self.m[rows] / self.nv)
+        return time.perf_counter() - t0
+
+
+def oracle_rate(p, seconds: float, seed: int = 0, max_calls: int = 16):
+    """Oracle fwd+bwd on seeded row samples for about `seconds`; (tokens/s, rows, secs, threads)."""
+    o = OracleSample(p, seed)
+    o.call()                     # first call pays BLAS start-up; not timed
+    calls, secs = 0, 0.0
+    while secs < seconds and calls < max_calls:
+        secs += o.call()
+        calls += 1
+    rows = calls * min(ORACLE_ROWS_PER_CALL, p.N)
+    return rows / secs, rows, secs, oracle_threads()
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    import torch
-
     from workloads import config_problem
     p = config_problem(args.workload, seed=args.seed, device="cpu", K=args.K, T=args.T)
-    import numpy as np
-
-    import oracle
-    W64 = p.W.double().numpy()
-    m = p.mask.numpy()
-    idx = p.idx.numpy()
-    t = p.t.double().numpy()
-    nv = max(int(m.sum()), 1)
-    rows_per_step = 64
-    rng = np.random.default_rng(args.seed)
+    o = OracleSample(p, args.seed)
     times = []
     for i in range(args.warmup + args.steps):
-        rows = np.sort(rng.choice(p.N, size=rows_per_step, replace=False))
-        Hs = p.H[rows].double().numpy()
-        t0 = time.perf_counter()
-        oracle.kd_forward(Hs, W64, idx[rows], t[rows], m[rows], p.T)
-        oracle.kd_backward(Hs, W64, idx[rows], t[rows], m[rows], p.T, m[rows] / nv)
+        dt = o.call()
         if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
+            times.append(dt)
     total = sum(times)
-    rate = rows_per_step * args.steps / total
-    try:
-        from threadpoolctl import threadpool_info
-        threads = max(int(d.get("num_threads", 1)) for d in threadpool_info())
-    except Exception:
-        threads = os.cpu_count()
-    sample = (f"{rows_per_step} seeded rows of {p.N} per step (fwd+bwd over the full V={p.V}); "
+    rows = min(ORACLE_ROWS_PER_CALL, p.N)
+    rate = rows * args.steps / total
+    sample = (f"{rows} seeded rows of {p.N} per step (fwd+bwd over the full V={p.V}); "
               f"the oracle is row-additive so rows/s is its tokens/s")
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": world,
@@ -318,10 +343,11 @@ def run_reference(args, rank, world):
         "ms_per_step": 1000.0 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_desc(p, args.chunk),
-        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "parallelism": "none (CPU oracle, rank 0 only)",
+        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "note": f"CPU fp64 oracle (numpy/OpenBLAS) on host cores; one step = {rows_per_step} rows",
+        "note": f"CPU fp64 oracle (numpy/OpenBLAS) on host cores; one step = {rows} rows",
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -330,37 +356,20 @@ def run_reference(args, rank, world):
 # ---------------------------------------------------------------------- CUDA path
 
 class Head:
-    """Device buffers and the fwd+bwd step of one replica."""
+    """One rank's device buffers and its step, through the product's
+    TokenShardedHead (all collectives are no-ops at world size 1)."""
 
-    def __init__(self, p, chunk):
-        import torch
-
-        from top_kl_loss_lm_b300 import binding
-        self.b = binding
+    def __init__(self, p, chunk, group=None):
+        from top_kl_loss_lm_b300.sharded import TokenShardedHead
         self.p = p
         self.chunk = chunk
-        dev = p.H.device
-        N, D, V, K = p.N, p.D, p.V, p.K
-        self.ws = torch.empty(binding.kd_topk_kl_workspace_size(N, D, V, K, chunk), dtype=torch.uint8,
-                              device=dev)
-        self.loss = torch.empty(N, dtype=torch.float32, device=dev)
-        self.lse = torch.empty(N, dtype=torch.float32, device=dev)
-        self.nv = torch.empty(1, dtype=torch.int64, device=dev)
-        self.dH = torch.empty_like(p.H)
-        self.dW = torch.empty(V, D, dtype=torch.float32, device=dev)
-        from workloads import mean_upstream_grad
-        self.g = mean_upstream_grad(p.mask).to(dev)
+        self.h = TokenShardedHead(p.N, p.D, p.V, p.K, p.T, p.H.device, chunk_tokens=chunk, group=group)
+        self.ws = self.h.ws
 
-    def step(self, H=None, idx=None, t=None, mask=None, g=None):
+    def step(self, H=None, idx=None, t=None, mask=None):
         p = self.p
-        H = p.H if H is None else H
-        idx = p.idx if idx is None else idx
-        t = p.t if t is None else t
-        mask = p.mask if mask is None else mask
-        g = self.g if g is None else g
-        self.b.kd_topk_kl_fwd(H, p.W, idx, t, mask, p.T, self.loss, self.lse, self.nv, self.ws)
-        self.b.kd_topk_kl_bwd(H, p.W, idx, t, mask, self.lse, g, p.T, self.chunk, False, self.dH,
-                              self.dW, self.ws)
+        return self.h.step(p.H if H is None else H, p.W, p.idx if idx is None else idx,
+                           p.t if t is None else t, p.mask if mask is None else mask)
 
 
 def run_ours(args, rank, world, local):
@@ -374,10 +383,28 @@ def run_ours(args, rank, world, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    # weak scaling: each rank holds its own N-token slice of the global batch
     p = config_problem(args.workload, seed=args.seed + rank, device=dev, K=args.K, T=args.T)
     head = Head(p, args.chunk)
     N, D, V = p.N, p.D, p.V
     flops_step = 8.0 * N * D * V
+    stream = torch.cuda.current_stream()
+
+    def timed(steps, fn):
+        """Device time (ms) of `steps` calls of fn on this stream, max over ranks."""
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        return max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     for _ in range(max(args.warmup, 3)):
         head.step()
@@ -385,35 +412,25 @@ def run_ours(args, rank, world, local):
     if st != 0:
         raise RuntimeError(f"device status {binding.STATUS.get(st, st)} after warm-up")
 
-    # ------------------------------------------------ device-timed region
+    # ------------------------------------------------ device-timed region (no per-kernel events)
     sampler = ClockSampler(local)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
     torch.cuda.reset_peak_memory_stats()
     sampler.start()
-    binding.kd_debug_profile(True)
-    stream = torch.cuda.current_stream()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        head.step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    ms = timed(args.steps, head.step)
     clocks = sampler.stop()
-    prof = binding.kd_debug_profile_read()
-    binding.kd_debug_profile(False)
-    ms = e0.elapsed_time(e1)
     st = binding.kd_get_status()
     if st != 0:
         raise RuntimeError(f"device status {binding.STATUS.get(st, st)} in the timed region")
     peak_mem = torch.cuda.max_memory_allocated()
-    ms = max_over_ranks(ms, world, dev)
     value = job_rate(N, world, args.steps, ms)
     tflops = job_rate(flops_step, world, args.steps, ms) / 1e12
+
+    # ------------------------------------------------ per-kernel times: a separate pass with events
+    prof_steps = min(args.steps, 5)
+    binding.kd_debug_profile(True)
+    prof_ms = timed(prof_steps, head.step)
+    prof = binding.kd_debug_profile_read()
+    binding.kd_debug_profile(False)
 
     # ------------------------------------------------ end to end from host buffers
     e2e = None
@@ -422,42 +439,33 @@ def run_ours(args, rank, world, local):
         hidx = p.idx.cpu().pin_memory()
         ht = p.t.cpu().pin_memory()
         hm = p.mask.cpu().pin_memory()
-        hg = head.g.cpu().pin_memory()
         hloss = torch.empty(N, dtype=torch.float32).pin_memory()
+        hsum = torch.empty(1, dtype=torch.float64).pin_memory()
         hnv = torch.empty(1, dtype=torch.int64).pin_memory()
         dH_in = torch.empty_like(p.H)
         didx = torch.empty_like(p.idx)
         dt = torch.empty_like(p.t)
         dm = torch.empty_like(p.mask)
-        dg = torch.empty_like(head.g)
 
         def e2e_step():
             dH_in.copy_(hH, non_blocking=True)
             didx.copy_(hidx, non_blocking=True)
             dt.copy_(ht, non_blocking=True)
             dm.copy_(hm, non_blocking=True)
-            dg.copy_(hg, non_blocking=True)
-            head.step(H=dH_in, idx=didx, t=dt, mask=dm, g=dg)
-            hloss.copy_(head.loss, non_blocking=True)
-            hnv.copy_(head.nv, non_blocking=True)
+            loss_sum, nv = head.step(H=dH_in, idx=didx, t=dt, mask=dm)
+            hloss.copy_(head.h.loss, non_blocking=True)
+            hsum.copy_(loss_sum, non_blocking=True)
+            hnv.copy_(nv, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
-        h2d = sum(x.numel() * x.element_size() for x in (hH, hidx, ht, hm, hg))
-        d2h = hloss.numel() * 4 + 8
+        ems = timed(args.steps, e2e_step)
+        h2d = sum(x.numel() * x.element_size() for x in (hH, hidx, ht, hm))
+        d2h = hloss.numel() * 4 + 8 + 8
         e2e = {"value": job_rate(N, world, args.steps, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "note": "H, teacher ids/logits, mask and upstream grad copied from pinned host memory "
-                       "each step; per-row loss and n_valid read back; W, dH, dW stay resident"}
+               "note": "H, teacher ids/logits and mask copied from pinned host memory each step; "
+                       "per-row loss, loss sum and n_valid read back; W, dH, dW stay resident"}
 
     if rank != 0:
         if world > 1:
@@ -470,45 +478,50 @@ def run_ours(args, rank, world, local):
     for c, (tot, n) in prof.items():
         if n == 0:
             continue
-        entry = {"ms_per_step": tot / args.steps, "launches_per_step": n / args.steps,
-                 "share": None}
+        entry = {"ms_per_step": tot / prof_steps, "launches_per_step": n / prof_steps, "share": None}
         if c in GEMM_CATS:
-            entry["tflops"] = 2.0 * N * D * V * args.steps / (tot / 1000.0) / 1e12
+            entry["tflops"] = 2.0 * N * D * V * prof_steps / (tot / 1000.0) / 1e12
         kernels[c] = entry
     total_k = sum(prof[c][0] for c in prof)
     for c in kernels:
         kernels[c]["share"] = prof[c][0] / total_k if total_k else None
     dom = max((c for c in kernels if c in GEMM_CATS), key=lambda c: prof[c][0])
     tot, n = prof[dom]
-    flops_per_launch = 2.0 * N * D * V * args.steps / n
+    flops_per_launch = 2.0 * N * D * V * prof_steps / n
     achieved = flops_per_launch / (tot / n / 1000.0) / 1e12
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = recorded_traffic(dom, p.name, args.chunk)
+    traffic = recorded_traffic(dom, p, args.chunk)
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sus,
                 "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": traffic,
-                "traffic_unit": "bytes per launch (dram read + write, ncu)",
+                "traffic_unit": "bytes per launch (dram read + write, ncu, scaled from the small "
+                                "capture in profiles/)",
                 "peak_kind": f"sustained bf16 dense ({peak_src}); kernel timed inside a long step",
                 "frac_of_burst": achieved / peak_burst,
-                "flops_per_launch": flops_per_launch}
+                "flops_per_launch": flops_per_launch,
+                "timing": f"per-launch CUDA events over a separate {prof_steps}-step pass "
+                          f"({prof_ms / prof_steps:.2f} ms/step with the events)"}
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         rate, nrows, secs, threads = oracle_rate(p, args.cpu_seconds, seed=args.seed)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{nrows} seeded rows of {N} (fwd+bwd over the full V={V}), {secs:.1f} s; "
-                         f"W converted to fp64 outside the timed part"}
+               "sample": f"{nrows} seeded rows of {N} in {ORACLE_ROWS_PER_CALL}-row calls "
+                         f"(fwd+bwd over the full V={V}), {secs:.1f} s; W converted to fp64 "
+                         f"outside the timed part"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_desc(p, args.chunk), parallelism=f"replicas x{world}"),
+        "config": workload_desc(p, args.chunk),
+        "parallelism": (f"dp{world}: token-sharded, {N} tokens per rank, dW / n_valid / loss sum "
+                        f"all-reduced (NCCL) inside the step") if world > 1 else "single GPU",
         "tflops": tflops, "frac_of_bf16_peak": {"burst": tflops / world / peak_burst,
                                                 "sustained": tflops / world / peak_sus},
         "peak_mem_gb": peak_mem / 1e9,
         "roofline": roofline, "kernels": kernels,
-        "gpu_launches": int(sum(n for _, n in prof.values())),
+        "gpu_launches": int(round(sum(n for _, n in prof.values()) * args.steps / prof_steps)),
         "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -617,7 +630,7 @@ def run_logits(args):
                              "N(0,4)+Gumbel sorted"},
         "roofline": {"bound": "hbm", "kernel": "kd_logits_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": recorded_traffic("logits", "gptoss_logits", 0),
+                     "traffic": None,
                      "traffic_unit": "bytes per launch (dram read + write, ncu)",
                      "peak_kind": f"HBM copy bandwidth ({src})",
                      "bytes_per_launch": per_launch},
@@ -716,7 +729,7 @@ def run_teacher_topk(args):
                    "inputs": "H ~ N(0,1), W ~ N(0,1/D) in bf16"},
         "roofline": {"bound": "tensor", "kernel": "topk_gemm", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": recorded_traffic("topk_gemm", "gptoss_teacher", 0),
+                     "traffic": None,
                      "peak_kind": f"sustained bf16 dense ({src})", "flops_per_step": flops},
         "kernels": {"topk_gemm": {"ms_per_step": gemm_ms}, "topk_select": {"ms_per_step": sel_ms}},
         "gpu_launches": int(sum(c[1] for c in prof.values())),
@@ -771,10 +784,8 @@ def run_sweep(args):
 def main():
     args = parse()
     if args.traffic_from:
-        name, chunk = (("gptoss_logits", 0) if args.logits else ("gptoss_teacher", 0)
-                       if args.teacher_topk else (args.workload, args.chunk))
-        rec = traffic_from_ncu_csv(args.traffic_from, name, chunk)
-        with open(traffic_file(name), "w") as f:
+        rec = traffic_from_ncu_csv(args.traffic_from.split(","), args.workload, args.chunk)
+        with open(TRAFFIC_RECORD, "w") as f:
             json.dump(rec, f, indent=1)
         print(json.dumps(rec))
         return 0

@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kMeanThreads)
                         double* __restrict__ loss_sum) {
   __shared__ double s_part[kMeanThreads];
   const int64_t nv = *n_valid;
-  const float g = nv > 0 ? static_cast<float>(1.0 / static_cast<double>(nv)) : 0.0f;
+  const float g = nv > 0 ? 1.0f / static_cast<float>(nv) : 0.0f;  // fp32, as torch's mask / n_valid
   double acc = 0.0;
   for (int64_t i = threadIdx.x; i < N; i += kMeanThreads) {
     const bool counted = (mask == nullptr) || (mask[i] != 0);

@@ -163,6 +163,11 @@ CONFIGS = {
     # small profiling case: same D and K as the gpt-oss head, W still larger than L2
     "profile_small": dict(N=4096, D=2880, V=32768, K=64, T=1.0, teacher="gumbel", mask="frac",
                           mask_frac=0.02),
+    # profiling case for DRAM traffic: the gpt-oss head's D, K and launch sizes (4,096
+    # rows per forward / dZ / dH launch, 8,192 tokens per dW launch: one store, one add)
+    # over a third of its vocabulary, ~3 GB on the device
+    "profile_medium": dict(N=16384, D=2880, V=65536, K=64, T=1.0, teacher="gumbel", mask="frac",
+                           mask_frac=0.02),
     "packed_qwen": dict(N=32768, D=4096, V=151936, K=64, T=1.0, teacher="gumbel", mask="packed",
                         garbage_masked=True),
 }
