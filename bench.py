@@ -100,31 +100,43 @@ def kernel_category(name: str):
 
 def traffic_from_ncu_csv(csv_paths, workload: str, chunk: int) -> dict:
     """DRAM bytes of every captured launch (dram__bytes_read.sum + dram__bytes_write.sum),
-    in capture order, from ncu --csv logs of the small profiling case."""
+    in capture order, from ncu csv exports of the small profiling case: either the long
+    form (--csv --metrics ..., one row per metric) or the wide form of
+    `ncu -i report --page raw --csv` (one row per launch, a units row under the header)."""
     import csv
-    launches = {}
+    scale_of = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9}
+    launches = []
     for path in csv_paths:
-        hdr = None
         with open(path) as f:
-            for r in csv.reader(f):
-                if r and r[0] == "ID":
-                    hdr = r
-                    continue
-                if hdr is None or len(r) < len(hdr):
-                    continue
+            rows = [r for r in csv.reader(f) if r]
+        start = next(i for i, r in enumerate(rows) if r[0] == "ID")
+        hdr = rows[start]
+        body = rows[start + 1:]
+        if "dram__bytes_read.sum" in hdr:      # wide
+            units = dict(zip(hdr, body[0]))
+            for r in body[1:]:
                 d = dict(zip(hdr, r))
                 cat = kernel_category(d["Kernel Name"])
-                if cat is None or d["Metric Name"] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                if cat is None:
                     continue
-                unit = d.get("Metric Unit", "byte").lower()
-                scale = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9}.get(unit, 1)
-                key = (path, int(d["ID"]))
-                e = launches.setdefault(key, {"cat": cat, "bytes": 0.0})
-                e["bytes"] += float(d["Metric Value"].replace(",", "")) * scale
+                b = sum(float(d[m].replace(",", "")) * scale_of.get(units[m].lower(), 1)
+                        for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"))
+                launches.append({"cat": cat, "bytes": b})
+            continue
+        per = {}
+        for r in body:                          # long
+            d = dict(zip(hdr, r))
+            cat = kernel_category(d.get("Kernel Name", ""))
+            if cat is None or d.get("Metric Name") not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                continue
+            e = per.setdefault(int(d["ID"]), {"cat": cat, "bytes": 0.0})
+            e["bytes"] += float(d["Metric Value"].replace(",", "")) * scale_of.get(
+                d.get("Metric Unit", "byte").lower(), 1)
+        launches += [per[k] for k in sorted(per)]
     from workloads import CONFIGS
     case = dict(CONFIGS[workload], chunk_tokens=chunk)
     return {"source_hash": kernel_source_hash(), "workload": workload, "case": case,
-            "launches": [launches[k] for k in sorted(launches)]}
+            "launches": launches}
 
 
 def recorded_traffic(kernel: str, p, chunk: int):
