@@ -211,9 +211,15 @@ kd_status kd_topk_kl_logits(const uint16_t* Z, int64_t ldz, const int32_t* topk_
  *   topk_idx [N x K] int32, topk_logit [N x K] fp32 outputs (raw logits; the
  *   loss applies the temperature).
  *   ws: kd_teacher_topk_workspace_size(N, D, V, K) bytes (one chunk of at most
- *   4,096 rows of fp32 logits, fixed in N beyond that).
+ *   4,096 rows of fp32 logits, plus for V >= 16,384 a sample of W's rows and
+ *   per-row candidate lists; fixed in N beyond 4,096 rows).
  * D a multiple of 8, 1 <= K <= min(V, 256). The logits are accumulated in fp32
- * on the tensor cores and the selection is exact on those fp32 values.
+ * on the tensor cores and the selection is exact on those fp32 values. For
+ * V >= 16,384 the chunk's logits are not written out: a strided sample of W's
+ * rows sets a threshold per row, the GEMM keeps the logits that reach it, and
+ * the K largest are picked from those; a row where the threshold keeps fewer
+ * than K or too many logits sends its chunk through the materialising path,
+ * so the result is the same either way.
  */
 size_t kd_teacher_topk_workspace_size(int64_t N, int D, int V, int K);
 

@@ -44,9 +44,10 @@ class Guarded:
 
 
 def _inputs_unchanged(before, after):
+    # byte for byte: masked rows carry NaN teacher logits, which never compare equal
     for name, (a, b) in zip(("H", "W", "idx", "t", "mask"), zip(before, after)):
-        assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
-                           b.view(torch.uint8) if b.dtype == torch.bfloat16 else b), f"input {name} written"
+        assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8)), \
+            f"input {name} written"
 
 
 def _fwd_bwd(p, chunk, accumulate=False):
@@ -124,7 +125,8 @@ def test_logits_writes_stay_inside_their_buffers(N, V, K, grad):
     assert binding.kd_get_status() == 0
 
 
-@pytest.mark.parametrize("N,D,V,K", [(300, 136, 1000, 16), (70, 64, 5000, 256), (4100, 72, 520, 1)])
+@pytest.mark.parametrize("N,D,V,K", [(300, 136, 1000, 16), (70, 64, 5000, 256), (4100, 72, 520, 1),
+                                     (301, 72, 20001 * 8 // 8, 100)])
 def test_teacher_topk_writes_stay_inside_their_buffers(N, D, V, K):
     p = make_problem(N, D, V, 1, 1.0, seed=54, device=DEV)
     ws = Guarded((binding.kd_teacher_topk_workspace_size(N, D, V, K),), torch.uint8)

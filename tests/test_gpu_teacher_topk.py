@@ -9,6 +9,11 @@ whose exact logit beats the smallest returned one by more than that error, and
 the returned values equal the oracle's top-K values within it. Ties are
 exercised on purpose (repeated rows of W, an all-zero hidden state); tied
 logits go to the smallest ids, so repeated calls return the same cache.
+
+Vocabularies of 16,384 and more take the fused path (a threshold per row from a
+strided sample of W's rows, the GEMM keeping only the logits that reach it);
+its fallback for rows whose threshold keeps too few or too many logits is
+forced on purpose below, and must give the same exact cache.
 """
 import numpy as np
 import pytest
@@ -108,6 +113,35 @@ def test_cache_feeds_the_loss():
     torch.cuda.synchronize()
     assert binding.kd_get_status() == 0
     assert float(loss.abs().max()) < 1e-4
+
+
+@pytest.mark.parametrize("K", [1, 100, 256])
+def test_fused_path_every_row(K):
+    H, W = _problem(300, 136, 20000, seed=7)
+    _check(H, W, K, *_run(H, W, K))
+
+
+def test_fused_path_over_several_chunks():
+    H, W = _problem(4096 + 123, 32, 16384 + 77, seed=8)
+    _check(H, W, 8, *_run(H, W, 8), rows=np.r_[0:64, 4060:4219])
+
+
+def test_fused_path_falls_back_exactly():
+    # V = 20,000 samples every 9th row of W. Row 5 is all ties (every logit 0: far
+    # more than the candidate list holds); on row 9 the sampled rows of W dominate
+    # (too few logits reach the threshold). Both force the chunk's exact fallback.
+    H, W = _problem(200, 64, 20000, seed=9)
+    H[5] = 0
+    Wf = W.float()
+    Wf[::9] *= 50.0
+    W2 = Wf.to(torch.bfloat16)
+    H2 = H.clone()
+    H2[9] = W2[0]  # z = <W[0], W[j]>: the sampled rows (x 50) tower over the rest
+    ids, vals = _run(H2, W2, 100)
+    _check(H2, W2, 100, ids, vals)
+    assert list(ids[5]) == list(range(100)) and np.all(vals[5] == 0)
+    ids2, vals2 = _run(H2, W2, 100)
+    assert np.array_equal(ids, ids2) and np.array_equal(vals, vals2)
 
 
 @pytest.mark.slow

@@ -21,7 +21,9 @@
 //             ids, rounded to bf16 and stored into the chunk's dZ buffer by TMA
 //   kEpiDh    dH tile (bf16, or fp32 partial per k-split)
 //   kEpiDw    dW tile, stored or added to the existing fp32 values
-//   kEpiPlain fp32 C tile (mainloop test hook)
+//   kEpiPlain fp32 C tile (mainloop test hook, the teacher's logits)
+//   kEpiCand  the teacher cache's candidates: every logit at or above its row's
+//             threshold is appended (value, id) to the row's candidate list
 // fp32 tiles (dW, plain, dH partials) are staged per warp in shared memory as
 // 32 x 16 boxes and written by TMA: a bulk-tensor store, or for an accumulating
 // dW a bulk-tensor add that L2 applies (one owner per tile, so no atomics race).
@@ -70,7 +72,7 @@ constexpr int kTmemCols = 512;
 constexpr int kGemmSmemBytes = Geo<false>::kSmemBytes > Geo<true>::kSmemBytes ? Geo<false>::kSmemBytes
                                                                                : Geo<true>::kSmemBytes;
 
-enum Epi : int { kEpiFwd = 0, kEpiDz = 1, kEpiDh = 2, kEpiDw = 3, kEpiPlain = 4 };
+enum Epi : int { kEpiFwd = 0, kEpiDz = 1, kEpiDh = 2, kEpiDw = 3, kEpiPlain = 4, kEpiCand = 5 };
 
 struct GemmArgs {
   Sched sched;
@@ -102,6 +104,15 @@ struct GemmArgs {
   int* status;
   uint64_t timeout_ns;
   int dh_partials;      // dH: fp32 partials through tmC even without a k-split
+  // kEpiCand: row r's threshold is thr[r * thr_stride + thr_stride - 1]; its list is
+  // cand_val / cand_id [r * cand_cap ...], cand_cnt[r] counts every logit that passed
+  const float* thr;
+  int thr_stride;
+  float* cand_val;
+  int32_t* cand_id;
+  int* cand_cnt;
+  int cand_cap;
+  const int* run_if;    // if set and *run_if == 0 the launch does nothing (a fallback)
 };
 
 // fp32 tiles leave through tmC (TMA store, or TMA add for an accumulating dW):
@@ -200,9 +211,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  // The forward's epilogue sends nothing through shared memory, so on a CTA pair
-  // its staging area becomes one more ring stage (same total shared memory).
-  constexpr bool kStaging = EPI != kEpiFwd || !PAIR;
+  // A fallback launch that is not needed returns at once (the flag is the same for
+  // both CTAs of a pair, so neither waits for the other).
+  if (args.run_if != nullptr && *args.run_if == 0) return;
+  // The forward's and the candidates' epilogues send nothing through shared memory,
+  // so on a CTA pair the staging area becomes one more ring stage (same total).
+  constexpr bool kStaging = (EPI != kEpiFwd && EPI != kEpiCand) || !PAIR;
   constexpr int kStages = kStaging ? G::kStages : G::kStages + kFwdExtraStages;
   static_assert(kStaging || kFwdExtraStages * G::kStageBytes <= kStagingBytes, "ring fits");
   uint8_t* staging = smem + kStages * G::kStageBytes;  // 1024-byte aligned
@@ -423,6 +437,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           cur = (ptr < K) ? __ldg(&args.pairs[rowK + ptr]) : make_int2(INT_MAX, 0);
         }
       }
+      float theta = INFINITY;  // kEpiCand: nothing passes on a row past the end
+      if (EPI == kEpiCand && row_ok) theta = __ldg(&args.thr[static_cast<int64_t>(row) * args.thr_stride +
+                                                             args.thr_stride - 1]);
       if (EPI == kEpiDw && args.accumulate != 0 && row_ok) {
         // The L2 add at the end of this unit reads the tile's current dW values:
         // start bringing this row's part in from DRAM while the main loop runs.
@@ -502,6 +519,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             send_chunk_bf16(&tmC, my_staging + (sent & 1) * kOutChunkBytes, dv, lane, col0, r0);
             ++sent;
+          } else if constexpr (EPI == kEpiCand) {
+            // a few hundred of a row's ~200K logits pass: test the chunk's maximum
+            // first, and append the passing logits (one global atomic each) only
+            // in the chunks that hold one
+            float mx = v[0];
+#pragma unroll
+            for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
+            if (mx >= theta) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {  // unrolled: v stays in registers
+              if (v[i] >= theta && col0 + i < args.Ncols) {
+                const int pos = atomicAdd(&args.cand_cnt[row], 1);
+                if (pos < args.cand_cap) {
+                  const int64_t o = static_cast<int64_t>(row) * args.cand_cap + pos;
+                  args.cand_val[o] = v[i];
+                  args.cand_id[o] = col0 + i;
+                }
+              }
+            }
+            }
           } else if (tma_out) {
             // dW, plain C, dH k-split partials: staged boxes, TMA store / add.
             // Boxes that start past the last row or column are not sent; the TMA

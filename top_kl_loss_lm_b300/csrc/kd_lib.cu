@@ -13,6 +13,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>  // header-only: ranges reach a profiler when one is attached
 
 #include <cmath>
 #include <cstdint>
@@ -85,8 +86,10 @@ unsigned long long current_ctx_id() {
   return id;
 }
 
-// Optional per-launch timing (test hook kd_debug_profile): a start/stop event
-// pair recorded on the launching stream around every kernel of the library.
+// Every kernel launch of the library sits in an NVTX range named for its
+// category (seen by Nsight tools; a no-op without one). Optional per-launch
+// timing (test hook kd_debug_profile): a start/stop event pair recorded on the
+// launching stream around every kernel of the library.
 enum ProfCat : int { kProfPrep = 0, kProfFwdGemm, kProfCombine, kProfDzGemm, kProfDhGemm, kProfDhSum,
                      kProfDwGemm, kProfLogits, kProfTopkGemm, kProfTopkSelect, kProfTranspose,
                      kProfCats };
@@ -98,10 +101,15 @@ struct Prof {
 };
 Prof g_prof;
 
+const char* const kProfNames[kProfCats] = {"kd prep", "kd fwd gemm", "kd combine", "kd dZ gemm",
+                                           "kd dH gemm", "kd dH sum", "kd dW gemm", "kd logits",
+                                           "kd topk gemm", "kd topk select", "kd transpose"};
+
 struct ProfScope {
   cudaStream_t s;
   int rec = -1;
   ProfScope(int c, cudaStream_t st) : s(st) {
+    nvtxRangePushA(kProfNames[c]);
     if (!g_prof.on) return;
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_prof.used * 2 + 2 > g_prof.ev.size()) {
@@ -120,6 +128,7 @@ struct ProfScope {
   }
   ~ProfScope() {
     if (rec >= 0) cudaEventRecord(g_prof.ev[2 * rec + 1], s);
+    nvtxRangePop();
   }
 };
 
@@ -997,9 +1006,81 @@ int select_blocks_per_sm() {
 }  // namespace
 }  // namespace kd
 
+namespace kd {
+namespace {
+// Vocabularies from this size on take the fused path: a threshold per row from a
+// strided sample of W's rows, then the full GEMM keeps only the logits at or
+// above it. Smaller ones materialise each chunk's logits and select from them.
+constexpr int kFusedTopkMinV = 16384;
+
+struct TopkPlan {
+  int64_t C = 0, ldz = 0;      // rows per chunk, row stride of the materialised logits
+  bool fused = false;
+  int64_t stride = 1, S = 0, lds = 0;  // sample: W rows 0, stride, 2*stride, ... (S of them)
+  int r = 0;                   // row threshold = the r-th largest sampled logit
+  size_t zc = 0, zs = 0, wsm = 0, thr = 0, cv = 0, ci = 0, cnt = 0, flag = 0, total = 0;
+};
+
+TopkPlan topk_plan(int64_t N, int D, int V, int K) {
+  TopkPlan P;
+  P.C = topk_chunk_rows(N);
+  P.ldz = topk_ld(V);
+  size_t off = 0;
+  P.zc = off;  // the materialised chunk: the small-vocabulary path and the fallback
+  off = align256(off + static_cast<size_t>(P.C) * P.ldz * sizeof(float));
+  P.fused = V >= kFusedTopkMinV;
+  if (P.fused) {
+    P.stride = V / 2048 < 32 ? (V / 2048 < 1 ? 1 : V / 2048) : 32;
+    P.S = cdiv(V, P.stride);
+    P.lds = topk_ld(static_cast<int>(P.S));
+    // lambda = the expected number of the row's top K in the sample; the threshold
+    // is the (lambda + 4 sqrt(lambda) + 8)-th largest sampled logit, so the kept set
+    // misses a top-K logit (and the chunk falls back) about once in 1e10 rows for a
+    // sample that behaves like a random one (12 at K = 100 left ~1e-4: one row in a
+    // chunk of 4,096 then sent about every second chunk to the fallback)
+    const int64_t lam = cdiv(static_cast<int64_t>(K) * P.S, V);
+    const int64_t want = lam + static_cast<int64_t>(std::ceil(4.0 * std::sqrt(static_cast<double>(lam)))) + 8;
+    P.r = static_cast<int>(want < P.S ? want : P.S);
+    if (P.r > kThrMaxRank) {  // cannot happen for K <= 256 and a sampling stride >= 8
+      P.fused = false;
+      P.total = off;
+      return P;
+    }
+    P.zs = off;
+    off = align256(off + static_cast<size_t>(P.C) * P.lds * sizeof(float));
+    P.wsm = off;
+    off = align256(off + static_cast<size_t>(P.S) * D * sizeof(uint16_t));
+    P.thr = off;
+    off = align256(off + static_cast<size_t>(P.C) * sizeof(float));
+    P.cv = off;
+    off = align256(off + static_cast<size_t>(P.C) * kCandCap * sizeof(float));
+    P.ci = off;
+    off = align256(off + static_cast<size_t>(P.C) * kCandCap * sizeof(int32_t));
+    P.cnt = off;
+    off = align256(off + static_cast<size_t>(P.C) * sizeof(int));
+    P.flag = off;
+    off = align256(off + sizeof(int));
+  }
+  P.total = off;
+  return P;
+}
+
+kd_status launch_select(const float* Z, int64_t ldz, int64_t rows, int V, int K, int32_t* idx,
+                        float* val, const int* run_if, const DevInfo* di, cudaStream_t s) {
+  // persistent: as many CTAs as are resident at once (each CTA loops over rows)
+  int64_t grid = static_cast<int64_t>(select_blocks_per_sm()) * di->num_sms;
+  if (grid > rows) grid = rows;
+  ProfScope ps(kProfTopkSelect, s);
+  kd_topk_select_kernel<<<static_cast<unsigned>(grid), kSelectThreads, 0, s>>>(Z, ldz, rows, V, K,
+                                                                              idx, val, run_if);
+  return cuda_check();
+}
+}  // namespace
+}  // namespace kd
+
 extern "C" size_t kd_teacher_topk_workspace_size(int64_t N, int D, int V, int K) {
   if (N < 0 || D <= 0 || D % 8 != 0 || V <= 0 || K < 1 || K > kSelectMaxK || K > V) return 0;
-  return align256(static_cast<size_t>(topk_chunk_rows(N)) * topk_ld(V) * sizeof(float));
+  return topk_plan(N, D, V, K).total;
 }
 
 extern "C" kd_status kd_teacher_topk(const uint16_t* H, const uint16_t* W, int64_t N, int D, int V,
@@ -1013,43 +1094,111 @@ extern "C" kd_status kd_teacher_topk(const uint16_t* H, const uint16_t* W, int64
   if (!aligned(H, 16) || !aligned(W, 16) || !aligned(ws, 256) || !aligned(topk_idx, 4) ||
       !aligned(topk_logit, 4))
     return KD_ERR_ALIGN;
-  if (ws_bytes < kd_teacher_topk_workspace_size(N, D, V, K)) return KD_ERR_WORKSPACE;
+  const TopkPlan P = topk_plan(N, D, V, K);
+  if (ws_bytes < P.total) return KD_ERR_WORKSPACE;
   kd_status st = KD_OK;
   const DevInfo* di = device_info(&st);
   if (!di) return st;
   if (!on_device(di, {H, W, topk_idx, topk_logit, ws})) return KD_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t C = topk_chunk_rows(N);
-  const int64_t ldz = topk_ld(V);
-  float* Zc = static_cast<float*>(ws);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* Zc = reinterpret_cast<float*>(w + P.zc);
   CUtensorMap mH, mW, mZ;
   if (!make_map(&mH, H, D, N, static_cast<uint64_t>(D) * 2, kBK, kBM) ||
       !make_map(&mW, W, D, V, static_cast<uint64_t>(D) * 2, kBK, Geo<kPair>::kBRows) ||
-      !make_out_map(&mZ, Zc, V, C, static_cast<uint64_t>(ldz) * 4))
+      !make_out_map(&mZ, Zc, V, P.C, static_cast<uint64_t>(P.ldz) * 4))
     return KD_ERR_CUDA;
   const int NB = static_cast<int>(cdiv(V, kBNMax));
   const int KB = static_cast<int>(cdiv(D, kBK));
-  for (int64_t c0 = 0; c0 < N; c0 += C) {
-    const int64_t rows = (N - c0) < C ? (N - c0) : C;
+
+  float* Zs = reinterpret_cast<float*>(w + P.zs);
+  uint16_t* Ws = reinterpret_cast<uint16_t*>(w + P.wsm);
+  float* thr = reinterpret_cast<float*>(w + P.thr);
+  float* cv = reinterpret_cast<float*>(w + P.cv);
+  int32_t* ci = reinterpret_cast<int32_t*>(w + P.ci);
+  int* cnt = reinterpret_cast<int*>(w + P.cnt);
+  int* flag = reinterpret_cast<int*>(w + P.flag);
+  CUtensorMap mWs, mZs;
+  if (P.fused) {
+    {
+      ProfScope ps(kProfTranspose, s);  // the sample of W's rows, once per call
+      const int64_t n = P.S * (D / 8);
+      int64_t blocks = cdiv(n, 256);
+      if (blocks > 8L * di->num_sms) blocks = 8L * di->num_sms;
+      kd_gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(W, P.stride, P.S, D, Ws);
+      if ((st = cuda_check()) != KD_OK) return st;
+    }
+    if (!make_map(&mWs, Ws, D, P.S, static_cast<uint64_t>(D) * 2, kBK, Geo<kPair>::kBRows) ||
+        !make_out_map(&mZs, Zs, P.S, P.C, static_cast<uint64_t>(P.lds) * 4))
+      return KD_ERR_CUDA;
+  }
+
+  for (int64_t c0 = 0; c0 < N; c0 += P.C) {
+    const int64_t rows = (N - c0) < P.C ? (N - c0) : P.C;
+    const int MB = static_cast<int>(cdiv(rows, kTileRows));
+    int32_t* out_idx = topk_idx + c0 * K;
+    float* out_val = topk_logit + c0 * K;
     GemmArgs a = base_args(di);
-    a.sched = make_panel_sched(static_cast<int>(cdiv(rows, kTileRows)), NB, KB, gemm_slots(di));
+    a.sched = make_panel_sched(MB, NB, KB, gemm_slots(di));
     a.M = static_cast<int>(rows);
     a.Ncols = V;
     a.BN = kBNMax;
     a.idesc = umma_idesc_bf16(kTileRows, kBNMax, false, false);
     a.a_row_off = static_cast<int>(c0);
+    if (P.fused) {
+      // 1. the sampled logits and each row's threshold (its r-th largest sampled logit)
+      GemmArgs sa = a;
+      sa.sched = make_panel_sched(MB, static_cast<int>(cdiv(P.S, kBNMax)), KB, gemm_slots(di));
+      sa.Ncols = static_cast<int>(P.S);
+      {
+        ProfScope ps(kProfTopkGemm, s);
+        if ((st = launch_gemm<kEpiPlain, false, false, kPair>(mH, mWs, mZs, sa, di, s)) != KD_OK)
+          return st;
+      }
+      {
+        int64_t grid = cdiv(rows, kThrWarps);
+        if (grid > 8L * di->num_sms) grid = 8L * di->num_sms;
+        ProfScope ps(kProfTopkSelect, s);
+        kd_row_threshold_kernel<<<static_cast<unsigned>(grid), kThrWarps * 32, 0, s>>>(
+            Zs, P.lds, rows, static_cast<int>(P.S), P.r, thr);
+        if ((st = cuda_check()) != KD_OK) return st;
+      }
+      // 2. the full GEMM keeps what reaches the threshold
+      if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(rows) * sizeof(int), s) != cudaSuccess ||
+          cudaMemsetAsync(flag, 0, sizeof(int), s) != cudaSuccess)
+        return KD_ERR_CUDA;
+      GemmArgs ca = a;
+      ca.thr = thr;
+      ca.thr_stride = 1;
+      ca.cand_val = cv;
+      ca.cand_id = ci;
+      ca.cand_cnt = cnt;
+      ca.cand_cap = kCandCap;
+      {
+        ProfScope ps(kProfTopkGemm, s);
+        if ((st = launch_gemm<kEpiCand, false, false, kPair>(mH, mW, mH, ca, di, s)) != KD_OK)
+          return st;
+      }
+      // 3. the K largest of each row's candidates; a row whose list is short or
+      //    overflowed raises the flag
+      {
+        int64_t grid = rows < 8L * di->num_sms ? rows : 8L * di->num_sms;
+        ProfScope ps(kProfTopkSelect, s);
+        kd_cand_select_kernel<<<static_cast<unsigned>(grid), kCandThreads, 0, s>>>(
+            cv, ci, cnt, kCandCap, rows, K, out_idx, out_val, flag);
+        if ((st = cuda_check()) != KD_OK) return st;
+      }
+      // 4. fallback for the chunk, run only if the flag is up: materialise and select
+      a.run_if = flag;
+    }
     {
       ProfScope ps(kProfTopkGemm, s);
       if ((st = launch_gemm<kEpiPlain, false, false, kPair>(mH, mW, mZ, a, di, s)) != KD_OK)
         return st;
     }
-    // persistent: as many CTAs as are resident at once (each CTA loops over rows)
-    int64_t grid = static_cast<int64_t>(select_blocks_per_sm()) * di->num_sms;
-    if (grid > rows) grid = rows;
-    ProfScope ps(kProfTopkSelect, s);
-    kd_topk_select_kernel<<<static_cast<unsigned>(grid), kSelectThreads, 0, s>>>(
-        Zc, ldz, rows, V, K, topk_idx + c0 * K, topk_logit + c0 * K);
-    if ((st = cuda_check()) != KD_OK) return st;
+    if ((st = launch_select(Zc, P.ldz, rows, V, K, out_idx, out_val, P.fused ? flag : nullptr, di,
+                            s)) != KD_OK)
+      return st;
   }
   return KD_OK;
 }

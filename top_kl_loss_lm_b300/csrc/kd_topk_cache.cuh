@@ -56,7 +56,9 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool acti
 
 __global__ void __launch_bounds__(kSelectThreads, 3)
     kd_topk_select_kernel(const float* __restrict__ Z, int64_t ldz, int64_t rows, int V, int K,
-                          int32_t* __restrict__ out_idx, float* __restrict__ out_val) {
+                          int32_t* __restrict__ out_idx, float* __restrict__ out_val,
+                          const int* __restrict__ run_if) {
+  if (run_if != nullptr && *run_if == 0) return;  // a fallback launch that is not needed
   __shared__ uint32_t hist[kSelectBins];
   __shared__ uint32_t warp_sum[kSelectWarps];
   __shared__ uint32_t s_bin, s_above;
@@ -301,6 +303,154 @@ __global__ void __launch_bounds__(kSelectThreads, 3)
       out_val[row * K + i] = key_float(ckey[i]);
     }
     __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ candidates from the GEMM
+//
+// The fused form of the cache (no chunk of logits written to memory): a strided
+// sample of W's rows gives each row a threshold (the r-th largest sampled logit,
+// r a little above K times the sampling rate), the full GEMM's epilogue keeps
+// every logit at or above it (kEpiCand), and kd_cand_select_kernel picks the K
+// largest of those. A row that kept fewer than K logits, or more than the list
+// holds, raises a flag that runs the materialising path for the chunk instead.
+
+// dst[i][:] = src[i * stride][:] for i < rows_out (bf16, D a multiple of 8).
+__global__ void __launch_bounds__(256)
+    kd_gather_rows_kernel(const uint16_t* __restrict__ src, int64_t stride, int64_t rows_out, int D,
+                          uint16_t* __restrict__ dst) {
+  const int64_t per_row = D / 8;
+  const int64_t n = rows_out * per_row;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / per_row, c = i - r * per_row;
+    reinterpret_cast<uint4*>(dst + r * D)[c] = __ldg(reinterpret_cast<const uint4*>(src + r * stride * D) + c);
+  }
+}
+
+constexpr int kCandCap = 2048;        // candidates kept per row
+constexpr int kCandThreads = 256;
+
+// One CTA per row (grid-stride): the row's candidates as 64-bit keys (logit key
+// high, ~id low), bitonic-sorted descending in shared memory, the first K written
+// out (descending logit, ascending id on ties: the order the cache promises). A
+// row with fewer than K or more than cap candidates sets *fail instead.
+__global__ void __launch_bounds__(kCandThreads)
+    kd_cand_select_kernel(const float* __restrict__ cand_val, const int32_t* __restrict__ cand_id,
+                          const int* __restrict__ cand_cnt, int cap, int64_t rows, int K,
+                          int32_t* __restrict__ out_idx, float* __restrict__ out_val,
+                          int* __restrict__ fail) {
+  __shared__ unsigned long long keys[kCandCap];
+  const int tid = threadIdx.x;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int cnt = cand_cnt[row];
+    if (cnt < K || cnt > cap) {
+      if (tid == 0) atomicExch(fail, 1);
+      continue;  // uniform across the block
+    }
+    int P = 1;
+    while (P < cnt) P <<= 1;
+    for (int i = tid; i < P; i += kCandThreads) {
+      unsigned long long k = 0ull;  // padding sorts last
+      if (i < cnt) {
+        const int64_t o = row * cap + i;
+        k = (static_cast<unsigned long long>(float_key(cand_val[o])) << 32) |
+            static_cast<unsigned long long>(~static_cast<uint32_t>(cand_id[o]));
+      }
+      keys[i] = k;
+    }
+    __syncthreads();
+    for (int size = 2; size <= P; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < P; i += kCandThreads) {
+          const int partner = i ^ stride;
+          if (partner > i) {
+            const bool desc = (i & size) == 0;
+            const unsigned long long a = keys[i], b = keys[partner];
+            if ((a > b) != desc && a != b) {
+              keys[i] = b;
+              keys[partner] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = tid; i < K; i += kCandThreads) {
+      const unsigned long long k = keys[i];
+      out_idx[row * K + i] = static_cast<int32_t>(~static_cast<uint32_t>(k & 0xFFFFFFFFull));
+      out_val[row * K + i] = key_float(static_cast<uint32_t>(k >> 32));
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ row thresholds
+//
+// thr[row] = the r-th largest of Z[row][0 .. n) (r <= 64), one warp per row and no
+// shared memory: the warp holds the 64 largest values seen so far in descending
+// order, position p in register p / 32 of lane p % 32. A batch of 32 new values
+// (one per lane) is skipped unless one of them beats the current 64th largest;
+// otherwise the batch is sorted (bitonic, across lanes) and merged: the element-
+// wise max of the list and the reversed batch holds the 64 largest of the union
+// as a bitonic sequence, which six compare-exchange stages sort again.
+constexpr int kThrMaxRank = 64;
+constexpr int kThrWarps = 8;
+
+__device__ __forceinline__ float cmpx_desc(float v, int lane, int stride, bool desc_block) {
+  // compare-exchange with lane ^ stride: the lower lane of the pair keeps the
+  // larger value when the block is descending
+  const float o = __shfl_xor_sync(0xffffffffu, v, stride);
+  const bool lower = (lane & stride) == 0;
+  return (lower == desc_block) ? fmaxf(v, o) : fminf(v, o);
+}
+
+__global__ void __launch_bounds__(kThrWarps * 32)
+    kd_row_threshold_kernel(const float* __restrict__ Z, int64_t ldz, int64_t rows, int n, int r,
+                            float* __restrict__ thr) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kThrWarps + (threadIdx.x >> 5);
+  const int64_t wstep = static_cast<int64_t>(gridDim.x) * kThrWarps;
+  for (int64_t row = warp0; row < rows; row += wstep) {
+    const float* z = Z + row * ldz;
+    float a0 = -INFINITY, a1 = -INFINITY;  // positions lane and 32 + lane
+    constexpr int kAhead = 8;              // batches loaded before the first is used
+    for (int base0 = 0; base0 < n; base0 += 32 * kAhead) {
+      float xs[kAhead];
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) {
+        const int j = base0 + 32 * u + lane;
+        xs[u] = j < n ? __ldg(z + j) : -INFINITY;
+      }
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) {
+      float x = xs[u];
+      const float last = __shfl_sync(0xffffffffu, a1, 31);  // the current 64th largest
+      if (__ballot_sync(0xffffffffu, x > last) == 0u) continue;
+      // sort the batch descending across the lanes
+#pragma unroll
+      for (int size = 2; size <= 32; size <<= 1) {
+        const bool desc_block = (lane & size) == 0 || size == 32;
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) x = cmpx_desc(x, lane, stride, desc_block);
+      }
+      // positions 32..63 against the batch reversed (positions 0..31 keep theirs:
+      // the padded half of the batch is -inf there)
+      a1 = fmaxf(a1, __shfl_sync(0xffffffffu, x, 31 - lane));
+      // bitonic sequence of 64 -> descending: stride 32 inside the lane, then 16..1
+      const float hi = fmaxf(a0, a1), lo = fminf(a0, a1);
+      a0 = hi;
+      a1 = lo;
+#pragma unroll
+      for (int stride = 16; stride > 0; stride >>= 1) {
+        a0 = cmpx_desc(a0, lane, stride, true);
+        a1 = cmpx_desc(a1, lane, stride, true);
+      }
+      }
+    }
+    const int p = r - 1;
+    const float t = __shfl_sync(0xffffffffu, p < 32 ? a0 : a1, p & 31);
+    if (lane == 0) thr[row] = t;
   }
 }
 
