@@ -68,7 +68,8 @@ def parse():
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "dram_traffic_profile_medium.json")
 KERNEL_SOURCES = ("kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h", "kd_logits.cuh", "kd_topk_cache.cuh")
 # template argument of kd_gemm_kernel -> category of the library's launch timing
-GEMM_EPI = {"0": "fwd_gemm", "1": "dz_gemm", "2": "dh_gemm", "3": "dw_gemm", "4": "topk_gemm"}
+GEMM_EPI = {"0": "fwd_gemm", "1": "dz_gemm", "2": "dh_gemm", "3": "dw_gemm", "4": "topk_gemm",
+            "5": "topk_gemm"}
 
 
 def kernel_source_hash() -> str:
@@ -92,7 +93,8 @@ def kernel_category(name: str):
     if m:
         return GEMM_EPI[m.group(1)]
     for key, cat in (("kd_logits_kernel", "logits"), ("kd_topk_select_kernel", "topk_select"),
-                     ("kd_transpose_kernel", "transpose")):
+                     ("kd_cand_select_kernel", "topk_select"), ("kd_row_threshold_kernel", "topk_select"),
+                     ("kd_transpose_kernel", "transpose"), ("kd_gather_rows_kernel", "transpose")):
         if key in name:
             return cat
     return None

@@ -59,8 +59,9 @@ kd_status kd_debug_schedule(int kind, int64_t rows, int64_t cols, int64_t depth,
  * events and returns, per category, the summed milliseconds and the launch
  * count (arrays of length n; categories: 0 prep, 1 forward GEMM, 2 combine,
  * 3 dZ GEMM, 4 dH GEMM, 5 dH split sum, 6 dW GEMM, 7 loss from logits,
- * 8 teacher-logit GEMM, 9 top-K selection, 10 transposes of W and H for the
- * backward), then clears the records.
+ * 8 teacher-logit GEMMs, 9 top-K selection and thresholds, 10 the backward's
+ * transposes of H and the teacher cache's gather of W rows), then clears the
+ * records.
  * Event objects are created on first use and kept for the process lifetime.
  */
 kd_status kd_debug_profile(int enable);

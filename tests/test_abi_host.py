@@ -72,6 +72,26 @@ def test_argument_errors_without_gpu(lib):
     assert lib.kd_get_status(None) in (3, 7)
 
 
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers: host-only argument checks")
+def test_shard_and_mean_grad_argument_errors_without_gpu(lib):
+    f = ctypes.c_float(1.0)
+
+    def fwd_shard(v0, Vs, V=16, parts=16):
+        return lib.kd_topk_kl_fwd_shard(16, 16, v0, Vs, V, 16, 16, None, 4, 8, 2, f, parts, 16, 16, 256,
+                                        1 << 20, None)
+    assert fwd_shard(8, 9) == 1      # the shard runs past V
+    assert fwd_shard(-1, 4) == 1
+    assert fwd_shard(0, 0) == 1
+    assert fwd_shard(0, 16, parts=4) == 2  # parts must be 8-byte aligned
+    assert fwd_shard(4, 8) in (3, 7)       # valid: reaches CUDA, finds no device
+    assert lib.kd_topk_kl_shard_merge(16, 0, 16, None, 4, f, 16, 16, None) == 1   # R = 0
+    assert lib.kd_topk_kl_shard_merge(16, 2, 16, None, 4, ctypes.c_float(0.0), 16, 16, None) == 1
+    assert lib.kd_topk_kl_mean_grad(16, None, 4, None, 16, 16, None) == 1         # no n_valid
+    assert lib.kd_topk_kl_mean_grad(16, None, 4, 16, None, None, None) == 1       # no output
+    assert lib.kd_topk_kl_bwd_shard(16, 16, 12, 8, 16, 16, 16, None, 16, 16, 4, 8, 2, f, 0, 0, 0,
+                                    16, 16, 256, 1 << 20, None) == 1             # past V
+
+
 def test_workspace_linear_in_tokens(lib):
     D, V, K = 2880, 201088, 64
     Ns = [4096, 16384, 65536, 131072, 262144]

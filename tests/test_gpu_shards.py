@@ -148,3 +148,36 @@ def test_gptoss_head_in_two_shards_sampled_rows():
     P.assert_rows_close(out["loss"].cpu().numpy()[rows], ref["loss"], "loss (sampled rows)")
     P.assert_lse_close(out["lse"].cpu().numpy()[rows], ref["lse"], "lse (sampled rows)")
     P.assert_grad_close(out["dH"].double().cpu().numpy()[rows], ref["dH"], "dH (sampled rows)")
+
+
+def test_sharded_steps_on_one_gpu_match_the_oracle():
+    # the product's step classes with world size 1 (no collectives): the
+    # token-sharded step's forward / mean gradient / backward, and the vocabulary
+    # step's shard forward / merge / shard backward over the whole vocabulary
+    from top_kl_loss_lm_b300 import sharded
+    p = make_problem(500, 136, 3000, 16, 1.2, seed=45, mask="frac", mask_frac=0.1,
+                     garbage_masked=True, device=DEV)
+    h = P.host(p)
+    nv = int(p.mask.sum().item())
+    g = p.mask.cpu().numpy().astype(np.float64) / nv
+    ref_loss, ref_lse, _ = oracle.kd_forward(h["H"], h["W"], h["idx"], h["t"], h["mask"], p.T)
+    ref_dH, ref_dW = oracle.kd_backward(h["H"], h["W"], h["idx"], h["t"], h["mask"], p.T, g)
+    ref_mean = oracle.mean_loss(ref_loss, nv)
+
+    tok = sharded.TokenShardedHead(p.N, p.D, p.V, p.K, p.T, DEV, chunk_tokens=256)
+    loss_sum, n_valid = tok.step(p.H, p.W, p.idx, p.t, p.mask)
+    assert int(n_valid.item()) == nv
+    assert abs(sharded.mean_loss(loss_sum, n_valid) - ref_mean) <= 1e-3 * abs(ref_mean)
+    P.assert_rows_close(tok.loss.cpu().numpy(), ref_loss, "token-sharded loss")
+    P.assert_grad_close(tok.dH.double().cpu().numpy(), ref_dH, "token-sharded dH")
+    P.assert_grad_close(tok.dW.double().cpu().numpy(), ref_dW, "token-sharded dW")
+
+    voc = sharded.VocabShardedHead(p.N, p.D, p.V, p.K, p.T, DEV, chunk_tokens=256)
+    assert (voc.v0, voc.v1) == (0, p.V)
+    loss_sum, n_valid = voc.step(p.H, p.W[voc.v0:voc.v1], p.idx, p.t, p.mask)
+    assert abs(sharded.mean_loss(loss_sum, n_valid) - ref_mean) <= 1e-3 * abs(ref_mean)
+    P.assert_rows_close(voc.loss.cpu().numpy(), ref_loss, "vocabulary-sharded loss")
+    P.assert_lse_close(voc.lse.cpu().numpy(), ref_lse, "vocabulary-sharded lse")
+    P.assert_grad_close(voc.dH.double().cpu().numpy(), ref_dH, "vocabulary-sharded dH")
+    P.assert_grad_close(voc.dW_shard.double().cpu().numpy(), ref_dW, "vocabulary-sharded dW")
+    assert binding.kd_get_status() == 0

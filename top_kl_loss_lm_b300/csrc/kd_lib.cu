@@ -307,7 +307,7 @@ int ksplit_that_fits(const Layout& L, int D, size_t ws_bytes, int wanted) {
 
 int wanted_ksplit(int64_t C_pad, int D, int V, int grid) {
   const int MB = static_cast<int>(C_pad / kTileRows);
-  const int bn = hidden_tile_width(D);
+  const int bn = mn_major_tile_width(D);  // dH's hidden tiles (B = W, MN-major)
   const int NBd = static_cast<int>(cdiv(D, bn));
   const int KB = static_cast<int>(cdiv(V, kBK));
   return choose_ksplit(static_cast<int64_t>(MB) * NBd, KB, grid);
@@ -1308,7 +1308,8 @@ extern "C" kd_status kd_debug_schedule(int kind, int64_t rows, int64_t cols, int
     NB = static_cast<int>(cdiv(cols, BN));
     sc = make_panel_sched(MB, NB, KB, num_sms);
   } else {
-    BN = hidden_tile_width(static_cast<int>(cols));
+    // dH reads W MN-major (256-wide hidden tiles), dW the group's H^T K-major (even tiles)
+    BN = kind == 1 ? mn_major_tile_width(static_cast<int>(cols)) : hidden_tile_width(static_cast<int>(cols));
     NB = static_cast<int>(cdiv(cols, BN));
     const int ks = (kind == 1) ? choose_ksplit(static_cast<int64_t>(MB) * NB, KB, num_sms) : 1;
     sc = make_tile_sched(MB, NB, KB, ks);
