@@ -67,10 +67,13 @@ typedef struct CUstream_st* kd_stream_t;
  * Bytes of device workspace that kd_topk_kl_fwd and kd_topk_kl_bwd need for
  * these sizes (one buffer serves both calls). The only vocabulary-sized parts
  * are two chunks of dZ (chunk_tokens x V bf16 each; one when N fits in one
- * chunk), so the size grows linearly in N and never as N x V. chunk_tokens is
- * the backward's row-chunk C (rounded up to a multiple of 256 internally; <= 0
- * selects 4096). Returns 0 for invalid sizes. Pure host arithmetic; safe
- * without a GPU.
+ * chunk); beside them the backward keeps the transposed hidden states of two
+ * chunks (D x 2 chunk_tokens bf16) and the k-split partials of dH (at most
+ * 8 x chunk_tokens x D fp32), all fixed in N, so the size grows linearly in N
+ * and never as N x V. chunk_tokens is the backward's row-chunk C (rounded up
+ * to a multiple of 256 internally; <= 0 selects 4096). Returns 0 for invalid
+ * sizes. Host arithmetic (it reads the current device's SM count when there
+ * is one); safe without a GPU.
  */
 size_t kd_topk_kl_workspace_size(int64_t N, int D, int V, int K, int64_t chunk_tokens);
 
