@@ -57,7 +57,9 @@ typedef enum {
   KD_ERR_WORKSPACE = 4,    /* ws_bytes smaller than kd_topk_kl_workspace_size() */
   KD_ERR_INDEX = 5,        /* device: a teacher id outside [0, V) at a counted row */
   KD_ERR_TIMEOUT = 6,      /* device: a bounded pipeline wait ran out; results invalid */
-  KD_ERR_CUDA = 7          /* a CUDA runtime/driver call failed */
+  KD_ERR_CUDA = 7,         /* a CUDA runtime/driver call failed */
+  KD_ERR_BOUNDS = 8        /* device, checked build only: a bounds check failed and the access
+                              was skipped (libkdtopk_checked.so; see the build's -DKD_CHECKED) */
 } kd_status;
 
 /* Opaque stream handle; pass a cudaStream_t. */

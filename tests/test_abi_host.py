@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         s = binding.kd_status_string(code)
         assert isinstance(s, str) and s
     assert binding.kd_status_string(0) == "ok"

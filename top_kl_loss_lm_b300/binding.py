@@ -31,6 +31,7 @@ __all__ = [
 STATUS = {
     0: "KD_OK", 1: "KD_ERR_ARG", 2: "KD_ERR_ALIGN", 3: "KD_ERR_UNSUPPORTED",
     4: "KD_ERR_WORKSPACE", 5: "KD_ERR_INDEX", 6: "KD_ERR_TIMEOUT", 7: "KD_ERR_CUDA",
+    8: "KD_ERR_BOUNDS",
 }
 
 _LIB = None

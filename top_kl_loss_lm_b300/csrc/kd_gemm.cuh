@@ -146,9 +146,9 @@ __device__ __forceinline__ void send_chunk(const CUtensorMap* map, uint8_t* buf,
   if (lane == 0) {
     for (int b = 0; b < boxes; ++b) {
       if (add)
-        tma_reduce_add_2d(map, buf + b * kOutBoxBytes, x0 + kOutBoxCols * b, y0);
+        tma_reduce_add_2d<4>(map, buf + b * kOutBoxBytes, x0 + kOutBoxCols * b, y0);
       else
-        tma_store_2d(map, buf + b * kOutBoxBytes, x0 + kOutBoxCols * b, y0);
+        tma_store_2d<4>(map, buf + b * kOutBoxBytes, x0 + kOutBoxCols * b, y0);
     }
     bulk_commit_group();
   }
@@ -198,7 +198,7 @@ __device__ __forceinline__ void send_chunk_bf16(const CUtensorMap* map, uint8_t*
   fence_proxy_async_shared();
   __syncwarp();
   if (lane == 0) {
-    tma_store_2d(map, buf, x0, y0);
+    tma_store_2d<2>(map, buf, x0, y0);
     bulk_commit_group();
   }
 }

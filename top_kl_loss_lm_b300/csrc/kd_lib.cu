@@ -32,8 +32,6 @@
 
 namespace kd {
 
-__device__ int g_kd_status;  // first device-side error since the last kd_get_status
-
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -1228,6 +1226,7 @@ extern "C" const char* kd_status_string(kd_status status) {
     case KD_ERR_INDEX: return "teacher id outside [0, V) at a counted row";
     case KD_ERR_TIMEOUT: return "bounded pipeline wait ran out; results are invalid";
     case KD_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case KD_ERR_BOUNDS: return "checked build: a device-side bounds check failed (access skipped)";
   }
   return "unknown status";
 }

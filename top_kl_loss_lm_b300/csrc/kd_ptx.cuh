@@ -8,6 +8,27 @@
 
 namespace kd {
 
+__device__ int g_kd_status;  // first device-side error since the last kd_get_status
+
+// ---------------------------------------------------------------- checked build
+// Built with KD_CHECKED (the library's checked build, a stand-in for a memory
+// sanitizer), every bulk-tensor copy checks its coordinates first: both >= 0 and
+// the innermost one a multiple of 16 bytes. A copy that fails is skipped and
+// status 8 (KD_ERR_BOUNDS) is recorded; nothing traps. A skipped load leaves its
+// barrier short, so the bounded wait behind it runs out as well.
+#ifdef KD_CHECKED
+__device__ __forceinline__ bool kd_check(bool ok) {
+  if (!ok) atomicCAS(&g_kd_status, 0, 8);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool kd_check(bool) { return true; }
+#endif
+
+__device__ __forceinline__ bool box_ok(int32_t x, int32_t y, int elem_bytes) {
+  return kd_check(x >= 0 && y >= 0 && (x * elem_bytes) % 16 == 0);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -120,9 +141,10 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 }
 
 // 2D tiled bulk-tensor load global -> shared, completion counted on `bar`.
-// x is the innermost (contiguous) coordinate in elements, y the row.
+// x is the innermost (contiguous) coordinate in elements, y the row (bf16 tensors).
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t x, int32_t y) {
+  if (!box_ok(x, y, 2)) return;
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
@@ -134,6 +156,7 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
 // counted on `mbar_cluster_addr`, which may be the peer CTA's barrier.
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map,
                                                  uint32_t mbar_cluster_addr, int32_t x, int32_t y) {
+  if (!box_ok(x, y, 2)) return;
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
@@ -160,18 +183,22 @@ __device__ __forceinline__ void bulk_store_1d(void* gdst, const void* smem_src, 
 
 // Shared -> global bulk-tensor store of one box, or element-wise add of the box
 // into global memory (the add is performed at L2). Both are tracked in this
-// thread's bulk async-group; x must be a multiple of 16 bytes of elements and
-// neither coordinate may be negative.
+// thread's bulk async-group; x must be a multiple of 16 bytes of elements (EB
+// bytes each) and neither coordinate may be negative.
+template <int EB>
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int32_t x,
                                              int32_t y) {
+  if (!box_ok(x, y, EB)) return;
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
           reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(smem_src))
       : "memory");
 }
 
+template <int EB>
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* smem_src,
                                                   int32_t x, int32_t y) {
+  if (!box_ok(x, y, EB)) return;
   asm volatile(
       "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::
           "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(smem_src))

@@ -258,8 +258,10 @@ __global__ void __launch_bounds__(kSelectThreads, 3)
       if (!ok) return;
       if (k > tau) {
         const uint32_t slot = atomicAdd(&n_gt, 1u);
-        ckey[slot] = k;
-        cidx[slot] = id;
+        if (kd_check(slot < n_above)) {  // exactly n_above keys lie above tau
+          ckey[slot] = k;
+          cidx[slot] = id;
+        }
       } else if (k == tau && ~static_cast<uint32_t>(id) >= id_cut) {
         const uint32_t e = atomicAdd(&n_eq, 1u);
         if (e < take_eq) {  // exactly take_eq qualify; the guard only bounds the slots
