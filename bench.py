@@ -171,6 +171,17 @@ def recorded_traffic(kernel: str, p, chunk: int):
     return per * p.V / case["V"]
 
 
+def issued_width_factor(kernel: str, D: int, V: int) -> float:
+    """Tensor-core work a GEMM issues per useful FLOP. Every tile is one MMA
+    instruction wide in its output columns, and an instruction narrower than 256
+    columns takes as long as a 256-wide one (240 and 256 measured equal; 11 x 256
+    tiles take 11/12 of the time of 12), so a launch costs ceil(n / 256) x 256
+    columns for n useful ones: the hidden size D for dH and dW (2,880 -> 3,072),
+    the vocabulary V for the forward and dZ."""
+    n = D if kernel in ("dh_gemm", "dw_gemm") else V
+    return (-(-n // 256) * 256) / n
+
+
 def dense_grid_bytes(n_tokens: int, vocab: int, bytes_per_elem: int) -> int:
     """Bytes of one dense tokens x vocabulary grid: what the fused head never allocates."""
     return int(n_tokens) * int(vocab) * int(bytes_per_elem)
@@ -518,6 +529,7 @@ def run_ours(args, rank, world, local):
         entry = {"ms_per_step": tot / prof_steps, "launches_per_step": n / prof_steps, "share": None}
         if c in GEMM_CATS:
             entry["tflops"] = 2.0 * N * D * V * prof_steps / (tot / 1000.0) / 1e12
+            entry["issued_per_useful"] = issued_width_factor(c, D, V)
         kernels[c] = entry
     total_k = sum(prof[c][0] for c in prof)
     for c in kernels:
@@ -536,6 +548,8 @@ def run_ours(args, rank, world, local):
                 "peak_kind": f"sustained bf16 dense ({peak_src}); kernel timed inside a long step",
                 "frac_of_burst": achieved / peak_burst,
                 "flops_per_launch": flops_per_launch,
+                "issued_per_useful": issued_width_factor(dom, D, V),
+                "frac_issued": achieved * issued_width_factor(dom, D, V) / peak_sus,
                 "timing": f"per-launch CUDA events over a second {prof_steps}-step pass right after "
                           f"the timed one ({prof_ms / prof_steps:.2f} ms/step with the events)"}
 
