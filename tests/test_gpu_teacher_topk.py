@@ -144,6 +144,21 @@ def test_fused_path_falls_back_exactly():
     assert np.array_equal(ids, ids2) and np.array_equal(vals, vals2)
 
 
+def test_fused_select_many_equal_candidates():
+    # Rows 1,000..1,600 of W repeat row 999, and row 3 of H points along it: that
+    # row's 602 largest logits are equal. All of them are candidates, more than the
+    # short sort after the histogram holds, so the row sorts its whole list; the K
+    # kept go to the smallest ids. Row 4 sees them among ordinary logits.
+    H, W = _problem(64, 64, 20000, seed=10)
+    W[1000:1601] = W[999]
+    H2 = H.clone()
+    H2[3] = W[999] * 4
+    ids, vals = _run(H2, W, 100)
+    _check(H2, W, 100, ids, vals)
+    assert list(ids[3]) == list(range(999, 1099))
+    assert np.all(vals[3] == vals[3][0])
+
+
 @pytest.mark.slow
 def test_gptoss_teacher_head_sampled_rows():
     # the pages cache the top 100 over the 201,088-token vocabulary

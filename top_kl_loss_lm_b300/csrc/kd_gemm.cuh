@@ -203,6 +203,61 @@ __device__ __forceinline__ void send_chunk_bf16(const CUtensorMap* map, uint8_t*
   }
 }
 
+// kEpiCand on one accumulator tile of this warp's 32 rows (lane = row). A few
+// hundred of a row's ~200K logits reach its threshold, so almost every 32 x 32
+// block of a tile holds one, and an atomic per passing logit would put several
+// L2 round trips per block on the epilogue's path. So a first pass over the
+// tile's TMEM chunks marks each row's passing columns (one bit mask per chunk),
+// one atomic per row reserves that many slots of the row's list, and a second
+// pass reads the chunks that hold any passing logit again and writes them.
+// Columns past the vocabulary's end never pass. cand_cnt counts every passing
+// logit, written or not, so a list that overflowed is seen by the select.
+__device__ __forceinline__ void cand_tile(uint32_t tacc, int col_tile, float theta, int row,
+                                          bool row_ok, const GemmArgs& args) {
+  uint32_t mask[kBNMax / 32];
+  int total = 0;
+#pragma unroll
+  for (int c = 0; c < kBNMax / 32; ++c) {
+    mask[c] = 0u;
+    const int col0 = col_tile + 32 * c;
+    if (32 * c < args.BN && col0 < args.Ncols) {  // warp-uniform
+      float v[32];
+      __syncwarp();
+      tmem_ld32(tacc + 32 * c, v);
+      uint32_t m = 0u;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) m |= (v[i] >= theta ? 1u : 0u) << i;
+      const int valid = args.Ncols - col0;
+      if (valid < 32) m &= (1u << valid) - 1u;
+      if (!row_ok) m = 0u;
+      mask[c] = m;
+      total += __popc(m);
+    }
+  }
+  if (!__any_sync(0xffffffffu, total > 0)) return;
+  int pos = 0;
+  if (total > 0) pos = atomicAdd(&args.cand_cnt[row], total);
+  const int64_t base = static_cast<int64_t>(row) * args.cand_cap;
+#pragma unroll
+  for (int c = 0; c < kBNMax / 32; ++c) {
+    if (!__any_sync(0xffffffffu, mask[c] != 0u)) continue;  // warp-uniform
+    float v[32];
+    __syncwarp();
+    tmem_ld32(tacc + 32 * c, v);
+    const uint32_t m = mask[c];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if ((m >> i) & 1u) {
+        if (pos < args.cand_cap) {
+          args.cand_val[base + pos] = v[i];
+          args.cand_id[base + pos] = col_tile + 32 * c + i;
+        }
+        ++pos;
+      }
+    }
+  }
+}
+
 template <int EPI, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -459,8 +514,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t tacc = lane_addr + static_cast<uint32_t>(acc * kBNMax);
         const int col_tile = nb * args.BN;
+        if constexpr (EPI == kEpiCand) cand_tile(tacc, col_tile, theta, row, row_ok, args);
 #pragma unroll 1
-        for (int c = 0; c < kBNMax / 32; ++c) {
+        for (int c = 0; c < (EPI == kEpiCand ? 0 : kBNMax / 32); ++c) {
           if (32 * c >= args.BN) break;
           const int col0 = col_tile + 32 * c;
           if (col0 >= args.Ncols) break;
@@ -519,26 +575,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             send_chunk_bf16(&tmC, my_staging + (sent & 1) * kOutChunkBytes, dv, lane, col0, r0);
             ++sent;
-          } else if constexpr (EPI == kEpiCand) {
-            // a few hundred of a row's ~200K logits pass: test the chunk's maximum
-            // first, and append the passing logits (one global atomic each) only
-            // in the chunks that hold one
-            float mx = v[0];
-#pragma unroll
-            for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
-            if (mx >= theta) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {  // unrolled: v stays in registers
-              if (v[i] >= theta && col0 + i < args.Ncols) {
-                const int pos = atomicAdd(&args.cand_cnt[row], 1);
-                if (pos < args.cand_cap) {
-                  const int64_t o = static_cast<int64_t>(row) * args.cand_cap + pos;
-                  args.cand_val[o] = v[i];
-                  args.cand_id[o] = col0 + i;
-                }
-              }
-            }
-            }
           } else if (tma_out) {
             // dW, plain C, dH k-split partials: staged boxes, TMA store / add.
             // Boxes that start past the last row or column are not sent; the TMA

@@ -333,53 +333,140 @@ __global__ void __launch_bounds__(256)
 constexpr int kCandCap = 2048;        // candidates kept per row
 constexpr int kCandThreads = 256;
 
-// One CTA per row (grid-stride): the row's candidates as 64-bit keys (logit key
-// high, ~id low), bitonic-sorted descending in shared memory, the first K written
-// out (descending logit, ascending id on ties: the order the cache promises). A
-// row with fewer than K or more than cap candidates sets *fail instead.
+constexpr int kCandBins = 1024;       // histogram bins over a row's key range
+constexpr int kCandSel = 512;         // keys kept for the final sort
+
+// Bitonic sort, descending, of keys[0 .. P) in shared memory (P a power of two).
+__device__ __forceinline__ void bitonic_desc(unsigned long long* keys, int P, int tid) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P; i += kCandThreads) {
+        const int partner = i ^ stride;
+        if (partner > i) {
+          const bool desc = (i & size) == 0;
+          const unsigned long long a = keys[i], b = keys[partner];
+          if ((a > b) != desc && a != b) {
+            keys[i] = b;
+            keys[partner] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// One CTA per row (grid-stride). The row's candidates become 64-bit keys (logit
+// key high, ~id low: distinct, and their descending order is the cache's order,
+// ties at equal logits going to the smaller id). Only the K largest are needed:
+// a histogram of the logit keys over the row's key range finds the bin that
+// holds the K-th largest, the keys in it and above it (K plus that bin's share,
+// a few on typical rows) are gathered and sorted, and the first K written out. A
+// row where more than kCandSel keys share that bin and those above (heavy ties)
+// sorts all its candidates instead. A row with fewer than K or more than cap
+// candidates sets *fail.
 __global__ void __launch_bounds__(kCandThreads)
     kd_cand_select_kernel(const float* __restrict__ cand_val, const int32_t* __restrict__ cand_id,
                           const int* __restrict__ cand_cnt, int cap, int64_t rows, int K,
                           int32_t* __restrict__ out_idx, float* __restrict__ out_val,
                           int* __restrict__ fail) {
   __shared__ unsigned long long keys[kCandCap];
-  const int tid = threadIdx.x;
+  __shared__ unsigned long long sel[kCandSel];
+  __shared__ int hist[kCandBins];
+  __shared__ uint32_t s_lo, s_hi;
+  __shared__ int s_bin, s_nsel, s_warp[kCandThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kPer = kCandBins / kCandThreads;  // bins a thread scans
+  static_assert(kCandBins % kCandThreads == 0, "every bin has one scanning thread");
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const int cnt = cand_cnt[row];
     if (cnt < K || cnt > cap) {
       if (tid == 0) atomicExch(fail, 1);
       continue;  // uniform across the block
     }
-    int P = 1;
-    while (P < cnt) P <<= 1;
-    for (int i = tid; i < P; i += kCandThreads) {
-      unsigned long long k = 0ull;  // padding sorts last
-      if (i < cnt) {
-        const int64_t o = row * cap + i;
-        k = (static_cast<unsigned long long>(float_key(cand_val[o])) << 32) |
-            static_cast<unsigned long long>(~static_cast<uint32_t>(cand_id[o]));
-      }
-      keys[i] = k;
+    if (tid == 0) {
+      s_lo = 0xFFFFFFFFu;
+      s_hi = 0u;
+      s_nsel = 0;
+    }
+    for (int i = tid; i < kCandBins; i += kCandThreads) hist[i] = 0;
+    __syncthreads();
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int i = tid; i < cnt; i += kCandThreads) {
+      const int64_t o = row * cap + i;
+      const uint32_t hk = float_key(cand_val[o]);
+      keys[i] = (static_cast<unsigned long long>(hk) << 32) |
+                static_cast<unsigned long long>(~static_cast<uint32_t>(cand_id[o]));
+      lo = min(lo, hk);
+      hi = max(hi, hk);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+    }
+    if (lane == 0) {
+      atomicMin(&s_lo, lo);
+      atomicMax(&s_hi, hi);
     }
     __syncthreads();
-    for (int size = 2; size <= P; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = tid; i < P; i += kCandThreads) {
-          const int partner = i ^ stride;
-          if (partner > i) {
-            const bool desc = (i & size) == 0;
-            const unsigned long long a = keys[i], b = keys[partner];
-            if ((a > b) != desc && a != b) {
-              keys[i] = b;
-              keys[partner] = a;
-            }
-          }
-        }
-        __syncthreads();
+    const uint32_t klo = s_lo;
+    int shift = 0;
+    while (((s_hi - klo) >> shift) >= static_cast<uint32_t>(kCandBins)) ++shift;
+    for (int i = tid; i < cnt; i += kCandThreads)
+      atomicAdd(&hist[(static_cast<uint32_t>(keys[i] >> 32) - klo) >> shift], 1);
+    __syncthreads();
+    // the bin b holding the K-th largest key: the highest b whose count together
+    // with the bins above it reaches K (suffix sums, high bins first)
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) local += hist[tid * kPer + j];
+    int suf = local;  // sum over this lane and the lanes above it in the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_down_sync(0xffffffffu, suf, off);
+      if (lane + off < 32) suf += n;
+    }
+    if (lane == 0) s_warp[warp] = suf;
+    __syncthreads();
+    int above = suf - local;  // keys in the bins of higher threads
+    for (int w = warp + 1; w < kCandThreads / 32; ++w) above += s_warp[w];
+    if (above < K && above + local >= K) {
+#pragma unroll
+      for (int j = kPer - 1; j >= 0; --j) {
+        const int h = hist[tid * kPer + j];
+        if (above < K && above + h >= K) s_bin = tid * kPer + j;
+        above += h;
       }
     }
-    for (int i = tid; i < K; i += kCandThreads) {
+    __syncthreads();
+    const uint32_t bmin = static_cast<uint32_t>(s_bin);
+    for (int i = tid; i < cnt; i += kCandThreads) {
       const unsigned long long k = keys[i];
+      if (((static_cast<uint32_t>(k >> 32) - klo) >> shift) >= bmin) {
+        const int slot = atomicAdd(&s_nsel, 1);
+        if (slot < kCandSel) sel[slot] = k;
+      }
+    }
+    __syncthreads();
+    const int nsel = s_nsel;
+    unsigned long long* src = sel;
+    if (nsel <= kCandSel) {
+      int P = 1;
+      while (P < nsel) P <<= 1;
+      for (int i = nsel + tid; i < P; i += kCandThreads) sel[i] = 0ull;  // padding sorts last
+      __syncthreads();
+      bitonic_desc(sel, P, tid);
+    } else {
+      int P = 1;
+      while (P < cnt) P <<= 1;
+      for (int i = cnt + tid; i < P; i += kCandThreads) keys[i] = 0ull;
+      __syncthreads();
+      bitonic_desc(keys, P, tid);
+      src = keys;
+    }
+    for (int i = tid; i < K; i += kCandThreads) {
+      const unsigned long long k = src[i];
       out_idx[row * K + i] = static_cast<int32_t>(~static_cast<uint32_t>(k & 0xFFFFFFFFull));
       out_val[row * K + i] = key_float(static_cast<uint32_t>(k >> 32));
     }
