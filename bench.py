@@ -66,7 +66,9 @@ def parse():
 
 
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "dram_traffic_profile_medium.json")
-KERNEL_SOURCES = ("kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h", "kd_logits.cuh", "kd_topk_cache.cuh")
+# the sources of the loss step's kernels (the logits and teacher-cache kernels
+# are not launched by the step, so their files do not invalidate its record)
+KERNEL_SOURCES = ("kd_lib.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_sched.h")
 # template argument of kd_gemm_kernel -> category of the library's launch timing
 GEMM_EPI = {"0": "fwd_gemm", "1": "dz_gemm", "2": "dh_gemm", "3": "dw_gemm", "4": "topk_gemm",
             "5": "topk_gemm"}

@@ -1157,8 +1157,12 @@ extern "C" kd_status kd_teacher_topk(const uint16_t* H, const uint16_t* W, int64
         int64_t grid = cdiv(rows, kThrWarps);
         if (grid > 8L * di->num_sms) grid = 8L * di->num_sms;
         ProfScope ps(kProfTopkSelect, s);
-        kd_row_threshold_kernel<<<static_cast<unsigned>(grid), kThrWarps * 32, 0, s>>>(
-            Zs, P.lds, rows, static_cast<int>(P.S), P.r, thr);
+        if (P.r <= 32)
+          kd_row_threshold_kernel<true><<<static_cast<unsigned>(grid), kThrWarps * 32, 0, s>>>(
+              Zs, P.lds, rows, static_cast<int>(P.S), P.r, thr);
+        else
+          kd_row_threshold_kernel<false><<<static_cast<unsigned>(grid), kThrWarps * 32, 0, s>>>(
+              Zs, P.lds, rows, static_cast<int>(P.S), P.r, thr);
         if ((st = cuda_check()) != KD_OK) return st;
       }
       // 2. the full GEMM keeps what reaches the threshold

@@ -494,12 +494,18 @@ __device__ __forceinline__ float cmpx_desc(float v, int lane, int stride, bool d
   return (lower == desc_block) ? fmaxf(v, o) : fminf(v, o);
 }
 
+// ONE_LIST (r <= 32): only the 32 largest are kept, one register per lane. A
+// batch is skipped unless a value in it beats the current r-th largest (nothing
+// below that can reach the final r-th place), which on a random row lets about
+// half the batches through compared with testing against the 64th.
+template <bool ONE_LIST>
 __global__ void __launch_bounds__(kThrWarps * 32)
     kd_row_threshold_kernel(const float* __restrict__ Z, int64_t ldz, int64_t rows, int n, int r,
                             float* __restrict__ thr) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kThrWarps + (threadIdx.x >> 5);
   const int64_t wstep = static_cast<int64_t>(gridDim.x) * kThrWarps;
+  const int p = r - 1;
   for (int64_t row = warp0; row < rows; row += wstep) {
     const float* z = Z + row * ldz;
     float a0 = -INFINITY, a1 = -INFINITY;  // positions lane and 32 + lane
@@ -513,32 +519,38 @@ __global__ void __launch_bounds__(kThrWarps * 32)
       }
 #pragma unroll
       for (int u = 0; u < kAhead; ++u) {
-      float x = xs[u];
-      const float last = __shfl_sync(0xffffffffu, a1, 31);  // the current 64th largest
-      if (__ballot_sync(0xffffffffu, x > last) == 0u) continue;
-      // sort the batch descending across the lanes
+        float x = xs[u];
+        const float rth = __shfl_sync(0xffffffffu, (ONE_LIST || p < 32) ? a0 : a1, p & 31);
+        if (__ballot_sync(0xffffffffu, x > rth) == 0u) continue;
+        // sort the batch descending across the lanes
 #pragma unroll
-      for (int size = 2; size <= 32; size <<= 1) {
-        const bool desc_block = (lane & size) == 0 || size == 32;
+        for (int size = 2; size <= 32; size <<= 1) {
+          const bool desc_block = (lane & size) == 0 || size == 32;
 #pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) x = cmpx_desc(x, lane, stride, desc_block);
-      }
-      // positions 32..63 against the batch reversed (positions 0..31 keep theirs:
-      // the padded half of the batch is -inf there)
-      a1 = fmaxf(a1, __shfl_sync(0xffffffffu, x, 31 - lane));
-      // bitonic sequence of 64 -> descending: stride 32 inside the lane, then 16..1
-      const float hi = fmaxf(a0, a1), lo = fminf(a0, a1);
-      a0 = hi;
-      a1 = lo;
+          for (int stride = size >> 1; stride > 0; stride >>= 1) x = cmpx_desc(x, lane, stride, desc_block);
+        }
+        if constexpr (ONE_LIST) {
+          // the 32 largest of the list and the batch, reversed: a bitonic sequence
+          a0 = fmaxf(a0, __shfl_sync(0xffffffffu, x, 31 - lane));
 #pragma unroll
-      for (int stride = 16; stride > 0; stride >>= 1) {
-        a0 = cmpx_desc(a0, lane, stride, true);
-        a1 = cmpx_desc(a1, lane, stride, true);
-      }
+          for (int stride = 16; stride > 0; stride >>= 1) a0 = cmpx_desc(a0, lane, stride, true);
+        } else {
+          // positions 32..63 against the batch reversed (positions 0..31 keep theirs:
+          // the padded half of the batch is -inf there)
+          a1 = fmaxf(a1, __shfl_sync(0xffffffffu, x, 31 - lane));
+          // bitonic sequence of 64 -> descending: stride 32 inside the lane, then 16..1
+          const float hi = fmaxf(a0, a1), lo = fminf(a0, a1);
+          a0 = hi;
+          a1 = lo;
+#pragma unroll
+          for (int stride = 16; stride > 0; stride >>= 1) {
+            a0 = cmpx_desc(a0, lane, stride, true);
+            a1 = cmpx_desc(a1, lane, stride, true);
+          }
+        }
       }
     }
-    const int p = r - 1;
-    const float t = __shfl_sync(0xffffffffu, p < 32 ? a0 : a1, p & 31);
+    const float t = __shfl_sync(0xffffffffu, (ONE_LIST || p < 32) ? a0 : a1, p & 31);
     if (lane == 0) thr[row] = t;
   }
 }
