@@ -177,7 +177,9 @@ __global__ void __launch_bounds__(NT + 32, NT <= 128 ? 4 : 2) kd_logits_kernel(c
       const uint16_t* zrow = buf(b);
 
       // ---- pass 1: online max / sum of exponentials, and the teacher's cross term
-      float2 ms = make_float2(-INFINITY, 0.0f);
+      // running (max, sum of exponentials) in base 2; the sum in two lanes, packed
+      float msx = -INFINITY;
+      uint64_t msy2 = f32x2(0.0f, 0.0f);
       float cross = 0.0f;
       int2 pr = make_int2(INT_MAX, 0);
       float zk = 0.0f;
@@ -190,12 +192,17 @@ __global__ void __launch_bounds__(NT + 32, NT <= 128 ? 4 : 2) kd_logits_kernel(c
           float mx = z[0];
 #pragma unroll
           for (int i = 1; i < 8; ++i) mx = fmaxf(mx, z[i]);
-          const float mnew = fmaxf(ms.x, mx * a.scale2);
-          float s = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) s += ex2_approx(fmaf(z[i], a.scale2, -mnew));
-          ms.y = ms.y * ex2_approx(ms.x - mnew) + s;
-          ms.x = mnew;
+          const float mnew = fmaxf(msx, mx * a.scale2);
+          // the eight arguments z*log2e/T - max as four packed FMAs, the sum as
+          // packed adds (the exponentials stay one MUFU instruction each)
+          const uint64_t s2 = f32x2(a.scale2, a.scale2), nm2 = f32x2(-mnew, -mnew);
+          const uint64_t e0 = ex2_f32x2(fma_f32x2(f32x2(z[0], z[1]), s2, nm2));
+          const uint64_t e1 = ex2_f32x2(fma_f32x2(f32x2(z[2], z[3]), s2, nm2));
+          const uint64_t e2 = ex2_f32x2(fma_f32x2(f32x2(z[4], z[5]), s2, nm2));
+          const uint64_t e3 = ex2_f32x2(fma_f32x2(f32x2(z[6], z[7]), s2, nm2));
+          const float c = ex2_approx(msx - mnew);
+          msy2 = fma_f32x2(msy2, f32x2(c, c), add_f32x2(add_f32x2(e0, e1), add_f32x2(e2, e3)));
+          msx = mnew;
         }
         // teacher entries ctid, ctid + NT, ...; the first one is kept for the
         // gradient's correction (with the gradient NT >= K, so that is every entry)
@@ -211,6 +218,12 @@ __global__ void __launch_bounds__(NT + 32, NT <= 128 ? 4 : 2) kd_logits_kernel(c
             }
           }
         }
+      }
+      float2 ms;
+      {
+        float ylo, yhi;
+        f32x2_split(msy2, ylo, yhi);
+        ms = make_float2(msx, ylo + yhi);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -271,9 +284,13 @@ __global__ void __launch_bounds__(NT + 32, NT <= 128 ? 4 : 2) kd_logits_kernel(c
           if (counted) {
             const float z[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                                 bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+            const uint64_t s2 = f32x2(a.scale2, a.scale2), nl2 = f32x2(-lse2, -lse2);
+            const uint64_t g2 = f32x2(gs, gs);
             float d[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) d[i] = gs * ex2_approx(fmaf(z[i], a.scale2, -lse2));
+            for (int i = 0; i < 8; i += 2)
+              f32x2_split(mul_f32x2(g2, ex2_f32x2(fma_f32x2(f32x2(z[i], z[i + 1]), s2, nl2))), d[i],
+                          d[i + 1]);
             w = make_uint4(f2_to_bf16x2(d[0], d[1]), f2_to_bf16x2(d[2], d[3]),
                            f2_to_bf16x2(d[4], d[5]), f2_to_bf16x2(d[6], d[7]));
           } else {
