@@ -826,6 +826,7 @@ namespace {
 inline int logits_slice(int V, int cl) { return static_cast<int>(cdiv(cdiv(V, cl), 64) * 64); }
 
 constexpr size_t kLogitsSmemLimit = 227 * 1024;
+static_assert(kMaxTopK <= kLogitsMaxK, "the logits kernel stages every teacher entry of a row");
 
 // Shape of the loss-from-logits kernel. With the gradient: the smallest cluster
 // whose slices, two row buffers each, let two CTAs of 256 compute threads share

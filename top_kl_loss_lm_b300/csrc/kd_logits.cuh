@@ -40,6 +40,8 @@ constexpr int kLogitsThreadsLossOnly = 128;  // loss only: lighter CTAs, four pe
 constexpr int kLogitsMaxWarps = kLogitsThreads / 32;
 constexpr int kLogitsMaxCluster = 8;
 constexpr int kLogitsMaxBuffers = 4;
+constexpr int kLogitsMaxK = 256;  // teacher entries per row (two per compute thread at most)
+static_assert(kLogitsMaxK <= 2 * kLogitsThreadsLossOnly, "a compute thread holds at most two entries");
 
 struct LogitsArgs {
   const uint16_t* Z;     // N x V bf16 logits, row stride ldz elements
@@ -65,6 +67,7 @@ __host__ __device__ constexpr size_t logits_smem_bytes(int Vs, int nbuf) {
   return static_cast<size_t>(nbuf) * Vs * 2      // row slices (bf16)
          + 2 * kLogitsMaxCluster * 16            // cluster partials, two parities
          + 2 * kLogitsMaxWarps * 16              // block reduction scratch, two parities
+         + 2 * kLogitsMaxK * 8                   // the row's teacher entries, two parities
          + (2 * kLogitsMaxBuffers + 2) * 8 + 16; // full / empty / exchange barriers, abort flag
 }
 
@@ -97,7 +100,8 @@ __global__ void __launch_bounds__(NT + 32, NT <= 128 ? 4 : 2) kd_logits_kernel(c
   auto buf = [&](int b) { return reinterpret_cast<uint16_t*>(smem + b * slice_bytes); };
   float4* exch = reinterpret_cast<float4*>(smem + NBUF * slice_bytes);  // [2][kLogitsMaxCluster]
   float4* red = exch + 2 * kLogitsMaxCluster;                          // [2][max warps]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kLogitsMaxWarps);
+  int2* spairs = reinterpret_cast<int2*>(red + 2 * kLogitsMaxWarps);    // [2][max K]
+  uint64_t* full = reinterpret_cast<uint64_t*>(spairs + 2 * kLogitsMaxK);
   uint64_t* empty = full + kLogitsMaxBuffers;
   uint64_t* xbar = empty + kLogitsMaxBuffers;                          // [2]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(xbar + 2);
@@ -171,6 +175,16 @@ __global__ void __launch_bounds__(NT + 32, NT <= 128 ? 4 : 2) kd_logits_kernel(c
       const int64_t row = cluster + j * nclusters;
       const int b = static_cast<int>(j % NBUF);
       const int par = static_cast<int>(j & 1);
+      // The row's teacher entries and per-row values are read from global memory
+      // here and used only after pass 1's vector loop, so their latency hides
+      // behind it; the entries also go to shared memory for pass 2.
+      int2 q0 = make_int2(INT_MAX, 0), q1 = make_int2(INT_MAX, 0);
+      if (ctid < K) q0 = __ldg(&a.pairs[row * K + ctid]);
+      if (ctid + NT < K) q1 = __ldg(&a.pairs[row * K + ctid + NT]);
+      const bool counted = (a.mask == nullptr) || (a.mask[row] != 0);
+      const float dl = grad ? __ldg(&a.dloss[row]) : 0.0f;
+      const float entr = (rank == 0 && ctid == 0) ? __ldg(&a.ent[row]) : 0.0f;
+      int2* sp = spairs + par * kLogitsMaxK;
       bool work = !*abort_flag &&
                   mbar_wait_bounded(&full[b], static_cast<uint32_t>((j / NBUF) & 1), abort_flag,
                                     a.timeout_ns, a.status, 6);
@@ -204,19 +218,23 @@ __global__ void __launch_bounds__(NT + 32, NT <= 128 ? 4 : 2) kd_logits_kernel(c
           msy2 = fma_f32x2(msy2, f32x2(c, c), add_f32x2(add_f32x2(e0, e1), add_f32x2(e2, e3)));
           msx = mnew;
         }
-        // teacher entries ctid, ctid + NT, ...; the first one is kept for the
+        // teacher entries ctid and ctid + NT; the first one is kept for the
         // gradient's correction (with the gradient NT >= K, so that is every entry)
-        for (int k = ctid; k < K; k += NT) {
-          const int2 q = __ldg(&a.pairs[row * K + k]);
-          if (q.x >= lo && q.x < lo + len) {
-            const float zq = __uint_as_float(static_cast<uint32_t>(zrow[q.x - lo]) << 16);
-            cross += __int_as_float(q.y) * zq;
-            if (k == ctid) {
-              pr = q;
-              zk = zq;
-              mine = true;
-            }
+        if (ctid < K) {
+          sp[ctid] = q0;
+          if (q0.x >= lo && q0.x < lo + len) {
+            const float zq = __uint_as_float(static_cast<uint32_t>(zrow[q0.x - lo]) << 16);
+            cross += __int_as_float(q0.y) * zq;
+            pr = q0;
+            zk = zq;
+            mine = true;
           }
+        }
+        if (ctid + NT < K) {
+          sp[ctid + NT] = q1;
+          if (q1.x >= lo && q1.x < lo + len)
+            cross += __int_as_float(q1.y) *
+                     __uint_as_float(static_cast<uint32_t>(zrow[q1.x - lo]) << 16);
         }
       }
       float2 ms;
@@ -265,18 +283,17 @@ __global__ void __launch_bounds__(NT + 32, NT <= 128 ? 4 : 2) kd_logits_kernel(c
         }
       }
       const float lse2 = rms.x + log2f(rms.y);
-      const bool counted = (a.mask == nullptr) || (a.mask[row] != 0);
       if (rank == 0 && ctid == 0 && work) {
         const double lse = static_cast<double>(lse2) * 0.6931471805599453;
         a.lse[row] = static_cast<float>(lse);
-        a.loss[row] = counted ? static_cast<float>(static_cast<double>(a.ent[row]) -
+        a.loss[row] = counted ? static_cast<float>(static_cast<double>(entr) -
                                                    static_cast<double>(rcross) * a.inv_T + lse)
                               : 0.0f;
       }
 
       // ---- pass 2: dZ in place (the copy driver stores it)
       if (grad && work) {
-        const float gs = counted ? a.dloss[row] * a.inv_T : 0.0f;
+        const float gs = counted ? dl * a.inv_T : 0.0f;
         uint16_t* drow = buf(b);
         for (int v = ctid; v < nvec; v += NT) {
           uint4* p = reinterpret_cast<uint4*>(drow + 8 * v);
@@ -299,10 +316,10 @@ __global__ void __launch_bounds__(NT + 32, NT <= 128 ? 4 : 2) kd_logits_kernel(c
           *p = w;
         }
         compute_sync<NT>();  // the vectors are written before single entries are corrected
-        if (counted && mine && (ctid == 0 || __ldg(&a.pairs[row * K + ctid - 1]).x != pr.x)) {
+        if (counted && mine && (ctid == 0 || sp[ctid - 1].x != pr.x)) {
           float P = __int_as_float(pr.y);  // merge a run of repeated ids
           for (int k2 = ctid + 1; k2 < K; ++k2) {
-            const int2 q = __ldg(&a.pairs[row * K + k2]);
+            const int2 q = sp[k2];
             if (q.x != pr.x) break;
             P += __int_as_float(q.y);
           }
