@@ -538,21 +538,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
             const float mnew = fmaxf(m2, mx * args.scale2);
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            // arguments and partial sums two lanes at a time (packed fp32x2); the four
+            // partial sums take the same elements in the same order as scalar code would
+            const uint64_t sc2 = f32x2(args.scale2, args.scale2), nm2 = f32x2(-mnew, -mnew);
+            uint64_t p01 = f32x2(0.f, 0.f), p23 = f32x2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-              a0 += ex2_approx(fmaf(v[i + 0], args.scale2, -mnew));
-              a1 += ex2_approx(fmaf(v[i + 1], args.scale2, -mnew));
-              a2 += ex2_approx(fmaf(v[i + 2], args.scale2, -mnew));
-              a3 += ex2_approx(fmaf(v[i + 3], args.scale2, -mnew));
+              p01 = add_f32x2(p01, ex2_f32x2(fma_f32x2(f32x2(v[i + 0], v[i + 1]), sc2, nm2)));
+              p23 = add_f32x2(p23, ex2_f32x2(fma_f32x2(f32x2(v[i + 2], v[i + 3]), sc2, nm2)));
             }
+            float a0, a1, a2, a3;
+            f32x2_split(p01, a0, a1);
+            f32x2_split(p23, a2, a3);
             s2 = s2 * ex2_approx(m2 - mnew) + ((a0 + a1) + (a2 + a3));
             m2 = mnew;
           } else if constexpr (EPI == kEpiDz) {
             float dv[32];
             if (dz_row) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) dv[i] = gs * ex2_approx(fmaf(v[i], args.scale2, -lse2));
+              for (int i = 0; i < 32; i += 2)
+                f32x2_split(mul_f32x2(f32x2(gs, gs), ex2_f32x2(fma_f32x2(f32x2(v[i], v[i + 1]),
+                                                                         f32x2(args.scale2, args.scale2),
+                                                                         f32x2(-lse2, -lse2)))),
+                            dv[i], dv[i + 1]);
               while (cur.x < col0 + 32) {
                 sub_at32(dv, cur.x - col0, gs * __int_as_float(cur.y));
                 ++ptr;
