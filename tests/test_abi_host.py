@@ -184,3 +184,14 @@ def test_binding_refuses_host_tensors_and_mixed_devices():
     assert binding.call_device(a, None, a) == torch.device("cuda", 0)
     with pytest.raises(ValueError, match="different devices"):
         binding.call_device(a, b)
+
+
+def test_issued_width_factor():
+    # a GEMM pays for its output columns in 256-wide MMA instructions: the hidden
+    # size for dH and dW, the vocabulary for the forward and dZ
+    import bench
+    assert bench.issued_width_factor("dw_gemm", 2880, 201088) == 3072 / 2880
+    assert bench.issued_width_factor("dh_gemm", 2880, 201088) == 3072 / 2880
+    assert bench.issued_width_factor("dw_gemm", 4096, 151936) == 1.0
+    assert bench.issued_width_factor("fwd_gemm", 2880, 201088) == 201216 / 201088
+    assert bench.issued_width_factor("dz_gemm", 4096, 151936) == 152064 / 151936
