@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(kCandThreads)
       s_lo = 0xFFFFFFFFu;
       s_hi = 0u;
       s_nsel = 0;
+      s_bin = 0;  // (every key) if no thread claimed a bin, which cnt >= K rules out
     }
     for (int i = tid; i < kCandBins; i += kCandThreads) hist[i] = 0;
     __syncthreads();
