@@ -198,6 +198,21 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def per_clock_fraction(achieved: float, peak: float, clocks, peaks) -> float | None:
+    """achieved / peak with both taken per MHz of SM clock: the kernel's rate at
+    the median SM clock sampled during the timed region against the sustained
+    peak at the median clock under load recorded with it. Under the power cap
+    the clock differs from box to box, while the work done per clock does not."""
+    try:
+        mhz = float(clocks["sm_mhz"])
+        peak_mhz = float(peaks["clocks_under_load"]["sm_mhz_median"])
+    except (KeyError, TypeError, ValueError):
+        return None
+    if mhz <= 0 or peak_mhz <= 0:
+        return None
+    return (achieved / mhz) / (peak / peak_mhz)
+
+
 def workload_desc(p, chunk):
     return {
         "workload": f"{p.name}: N={p.N} tokens, D={p.D}, V={p.V}, K={p.K}, T={p.T}",
@@ -552,6 +567,7 @@ def run_ours(args, rank, world, local):
                 "flops_per_launch": flops_per_launch,
                 "issued_per_useful": issued_width_factor(dom, D, V),
                 "frac_issued": achieved * issued_width_factor(dom, D, V) / peak_sus,
+                "frac_per_clock": per_clock_fraction(achieved, peak_sus, clocks, peaks),
                 "timing": f"per-launch CUDA events over a second {prof_steps}-step pass right after "
                           f"the timed one ({prof_ms / prof_steps:.2f} ms/step with the events)"}
 

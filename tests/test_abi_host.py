@@ -195,3 +195,14 @@ def test_issued_width_factor():
     assert bench.issued_width_factor("dw_gemm", 4096, 151936) == 1.0
     assert bench.issued_width_factor("fwd_gemm", 2880, 201088) == 201216 / 201088
     assert bench.issued_width_factor("dz_gemm", 4096, 151936) == 152064 / 151936
+
+
+def test_per_clock_fraction():
+    # the same work per clock gives the same fraction on a slower-clocked box
+    import bench
+    peaks = {"clocks_under_load": {"sm_mhz_median": 1200.0}}
+    assert bench.per_clock_fraction(1300.0, 1400.0, {"sm_mhz": 1200.0}, peaks) == 1300.0 / 1400.0
+    slow = bench.per_clock_fraction(1300.0 * 1100 / 1200, 1400.0, {"sm_mhz": 1100.0}, peaks)
+    assert abs(slow - 1300.0 / 1400.0) < 1e-12
+    assert bench.per_clock_fraction(1300.0, 1400.0, None, peaks) is None
+    assert bench.per_clock_fraction(1300.0, 1400.0, {"sm_mhz": 1200.0}, {}) is None
