@@ -798,6 +798,7 @@ def run_teacher_topk(args):
                    "inputs": "H ~ N(0,1), W ~ N(0,1/D) in bf16"},
         "roofline": {"bound": "tensor", "kernel": "topk_gemm", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
+                     "frac_per_clock": per_clock_fraction(achieved, peak, clocks, peaks),
                      "traffic": None,
                      "peak_kind": f"sustained bf16 dense ({src})", "flops_per_step": flops},
         "kernels": {"topk_gemm": {"ms_per_step": gemm_ms}, "topk_select": {"ms_per_step": sel_ms}},
