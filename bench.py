@@ -202,8 +202,11 @@ def per_clock_fraction(achieved: float, peak: float, clocks, peaks) -> float | N
     """achieved / peak with both taken per MHz of SM clock: the kernel's rate at
     the median SM clock sampled during the timed region against the sustained
     peak at the median clock under load recorded with it. Under the power cap
-    the clock differs from box to box, while the work done per clock does not."""
+    the clock differs from box to box, while the work done per clock does not.
+    None when the timed region was too short for five clock samples."""
     try:
+        if int(clocks.get("samples", 0)) < 5:
+            return None
         mhz = float(clocks["sm_mhz"])
         peak_mhz = float(peaks["clocks_under_load"]["sm_mhz_median"])
     except (KeyError, TypeError, ValueError):

@@ -201,9 +201,10 @@ def test_per_clock_fraction():
     # the same work per clock gives the same fraction on a slower-clocked box
     import bench
     peaks = {"clocks_under_load": {"sm_mhz_median": 1200.0}}
-    same = bench.per_clock_fraction(1300.0, 1400.0, {"sm_mhz": 1200.0}, peaks)
+    same = bench.per_clock_fraction(1300.0, 1400.0, {"sm_mhz": 1200.0, "samples": 9}, peaks)
     assert abs(same - 1300.0 / 1400.0) < 1e-12
-    slow = bench.per_clock_fraction(1300.0 * 1100 / 1200, 1400.0, {"sm_mhz": 1100.0}, peaks)
+    slow = bench.per_clock_fraction(1300.0 * 1100 / 1200, 1400.0, {"sm_mhz": 1100.0, "samples": 9}, peaks)
     assert abs(slow - 1300.0 / 1400.0) < 1e-12
     assert bench.per_clock_fraction(1300.0, 1400.0, None, peaks) is None
-    assert bench.per_clock_fraction(1300.0, 1400.0, {"sm_mhz": 1200.0}, {}) is None
+    assert bench.per_clock_fraction(1300.0, 1400.0, {"sm_mhz": 1200.0, "samples": 9}, {}) is None
+    assert bench.per_clock_fraction(1300.0, 1400.0, {"sm_mhz": 1200.0, "samples": 2}, peaks) is None
