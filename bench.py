@@ -209,7 +209,7 @@ def per_clock_fraction(achieved: float, peak: float, clocks, peaks) -> float | N
             return None
         mhz = float(clocks["sm_mhz"])
         peak_mhz = float(peaks["clocks_under_load"]["sm_mhz_median"])
-    except (KeyError, TypeError, ValueError):
+    except (AttributeError, KeyError, TypeError, ValueError):
         return None
     if mhz <= 0 or peak_mhz <= 0:
         return None
