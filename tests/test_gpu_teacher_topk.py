@@ -168,3 +168,14 @@ def test_gptoss_teacher_head_sampled_rows():
     rng = np.random.default_rng(0)
     rows = np.unique(np.concatenate([rng.choice(H.shape[0], 24, replace=False), [0, H.shape[0] - 1]]))
     _check(H, W, K, ids, vals, rows=rows)
+
+
+@pytest.mark.slow
+def test_gptoss_teacher_head_k256_sampled_rows():
+    # the largest K the cache supports over the full vocabulary, with a ragged last chunk
+    H, W = _problem(2 * 4096 + 300, 2880, 201088, seed=16)
+    K = 256
+    ids, vals = _run(H, W, K)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([rng.choice(H.shape[0], 20, replace=False), [0, 4095, 4096, H.shape[0] - 1]]))
+    _check(H, W, K, ids, vals, rows=rows)
