@@ -154,11 +154,19 @@ __device__ __forceinline__ void send_chunk(const CUtensorMap* map, uint8_t* buf,
   }
 }
 
+// v[j] for a j known only at run time, without indexing the register array (which
+// would put it in local memory): a tree of selects on the bits of j.
 __device__ __forceinline__ float select32(const float (&v)[32], int j) {
-  float r = v[0];
+  float a[16], b[8], c[4], d[2];
 #pragma unroll
-  for (int i = 1; i < 32; ++i) r = (j == i) ? v[i] : r;
-  return r;
+  for (int i = 0; i < 16; ++i) a[i] = (j & 1) ? v[2 * i + 1] : v[2 * i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) b[i] = (j & 2) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = (j & 4) ? b[2 * i + 1] : b[2 * i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) d[i] = (j & 8) ? c[2 * i + 1] : c[2 * i];
+  return (j & 16) ? d[1] : d[0];
 }
 
 __device__ __forceinline__ void sub_at32(float (&v)[32], int j, float x) {
@@ -244,15 +252,19 @@ __device__ __forceinline__ void cand_tile(uint32_t tacc, int col_tile, float the
     float v[32];
     __syncwarp();
     tmem_ld32(tacc + 32 * c, v);
-    const uint32_t m = mask[c];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if ((m >> i) & 1u) {
+    // one iteration per passing logit of the lane that has the most in this chunk
+    uint32_t m = mask[c];
+    while (__any_sync(0xffffffffu, m != 0u)) {
+      const bool has = m != 0u;
+      const int i = has ? __ffs(m) - 1 : 0;
+      const float val = select32(v, i);
+      if (has) {
         if (pos < args.cand_cap) {
-          args.cand_val[base + pos] = v[i];
+          args.cand_val[base + pos] = val;
           args.cand_id[base + pos] = col_tile + 32 * c + i;
         }
         ++pos;
+        m &= m - 1u;
       }
     }
   }
